@@ -1,0 +1,505 @@
+#!/usr/bin/env python3
+"""Benchmark of the NVFP4 W4A16 linear layer on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-extras]
+
+Prints ONE JSON line.  A step is one pass of the layer over one batch of the
+headline workload (decode GEMV over the fused MLP gate+up projection:
+M=1, K=5120, N=34816); ``value`` is algorithmic bytes per step / time per
+step (GB/s), inputs resident in HBM, K steps timed with CUDA events between
+barriers + device synchronisations.  Weights are rotated over enough copies
+that the rotated set exceeds twice the L2 cache, so every step streams its
+weights from HBM.
+
+The other workloads (verify, M=32 layer, prefill with and without SwiGLU)
+are timed the same way and reported under "workloads".
+
+--impl reference times the CPU oracle (the reference arm of this build) on
+the host cores, on a bounded sample of the same workload per step.
+
+Multi-GPU (torchrun): every rank runs an independent replica on its own GPU
+(the layer has no exchange step); value = all ranks' bytes / max rank time.
+"""
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "NVFP4 W4A16 linear: GB/s (M≤32) & TFLOPS (M=8192), % of GB300 roofline"
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+HEADLINE = "decode_gate_up"
+
+
+# ----------------------------------------------------------------- helpers
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(
+            p.get("bf16_tflops_sustained", p["bf16_tflops"])), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "nvfp4_block_scaled_linear_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+        e = t[kernel][workload]
+        if e.get("source_hash") == kernel_source_hash():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle sampler over the benchmark's lifetime."""
+    FIELDS = ("clocks.sm,clocks.max.sm,utilization.gpu,power.draw,"
+              "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index, period_ms=50):
+        self.index = index
+        self.period_ms = period_ms
+        self.proc = None
+        self.lines = []
+        self.windows = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=timestamp," + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", str(self.period_ms)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._reader, daemon=True).start()
+        except Exception:
+            self.proc = None
+
+    def _reader(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, t0, t1):
+        self.windows.append((t0, t1))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                rows.append((ts, float(parts[1]), float(parts[2]), float(parts[3]), parts[5:]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        inwin = [r for r in rows if any(a - 0.05 <= r[0] <= b + 0.05 for a, b in self.windows)]
+        loaded = [r for r in inwin if r[3] > 0] or inwin or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in loaded:
+            for n, v in zip(names, r[4][1:5]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": float(np.median([r[1] for r in loaded])),
+                "sm_max_mhz": float(max(r[2] for r in loaded)),
+                "reasons": sorted(reasons), "samples": len(loaded)}
+
+
+# ----------------------------------------------------------------- distributed
+def dist_setup(n_gpus):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def aggregate_max(value, world):
+    """Max of a float over ranks (the slowest rank's time)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) \
+        if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(units_per_rank, max_seconds, world):
+    return units_per_rank * world / max_seconds
+
+
+# ----------------------------------------------------------------- GPU arm
+class Case:
+    """Device-resident inputs of one workload, with rotated weight copies."""
+
+    def __init__(self, name, lib, dev, min_rotated_bytes=2 * L2_BYTES):
+        import torch
+        from nvfp4_block_scaled_linear_gb300.inputs import WORKLOADS, algorithmic_bytes, flops
+        self.w = WORKLOADS[name]
+        self.name = name
+        self.lib = lib
+        self.flags = lib.FLAG_SWIGLU if self.w.swiglu else 0
+        self.linears = self.w.draw()
+        self.bytes = sum(algorithmic_bytes(t.M, t.N, t.K, self.w.swiglu) for t in self.linears)
+        self.flops = sum(flops(t.M, t.N, t.K) for t in self.linears)
+        per_copy = sum(t.w_packed.nbytes + t.w_scale.nbytes for t in self.linears)
+        act = sum(t.x_bits.nbytes for t in self.linears)
+        total = per_copy + act
+        self.copies = 1 if total >= min_rotated_bytes else int(np.ceil(min_rotated_bytes / total))
+        self.x = [torch.from_numpy(t.x_bits.view(np.int16)).view(torch.bfloat16).to(dev)
+                  for t in self.linears]
+        self.wp = [[torch.from_numpy(t.w_packed).to(dev) for t in self.linears]
+                   for _ in range(self.copies)]
+        self.ws = [[torch.from_numpy(t.w_scale).to(dev) for t in self.linears]
+                   for _ in range(self.copies)]
+        n_out = [t.N // 2 if self.w.swiglu else t.N for t in self.linears]
+        self.y = [torch.empty((t.M, n), dtype=torch.bfloat16, device=dev)
+                  for t, n in zip(self.linears, n_out)]
+        self.rotated_bytes = self.copies * per_copy + act
+        self.launches_per_step = len(self.linears)
+        self.kernel = lib.choose_plan(self.linears[0].M, self.linears[0].N, self.linears[0].K,
+                                      self.flags)
+
+    def step(self, i, stream, events=None):
+        c = i % self.copies
+        for j, t in enumerate(self.linears):
+            if events is not None:
+                events[0].record(stream)
+            self.lib.linear_ex(self.x[j], self.wp[c][j], self.ws[c][j], float(t.global_scale),
+                               self.flags, out=self.y[j], stream=stream)
+            if events is not None:
+                events[1].record(stream)
+
+    def l2_note(self):
+        if self.copies > 1:
+            return "rotating %d weight copies (%d MB > 2x L2)" % (self.copies,
+                                                                  self.rotated_bytes >> 20)
+        return "inputs larger than L2 (%d MB)" % (self.rotated_bytes >> 20)
+
+
+def time_case(case, steps, warmup, stream, world, sampler=None, per_launch=True):
+    import torch
+    for i in range(warmup):
+        case.step(i, stream)
+    torch.cuda.synchronize()
+    n_l = case.launches_per_step
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps * n_l)] if per_launch else None
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    wall0 = time.time()
+    t_start.record(stream)
+    for i in range(steps):
+        if per_launch:
+            for j, t in enumerate(case.linears):
+                a, b = ev[i * n_l + j]
+                a.record(stream)
+                case.lib.linear_ex(case.x[j], case.wp[i % case.copies][j],
+                                   case.ws[i % case.copies][j], float(t.global_scale),
+                                   case.flags, out=case.y[j], stream=stream)
+                b.record(stream)
+        else:
+            case.step(i, stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    wall1 = time.time()
+    if sampler:
+        sampler.mark(wall0, wall1)
+    total_ms = t_start.elapsed_time(t_end)
+    launch_ms = None
+    if per_launch:
+        # per linear: mean launch duration
+        launch_ms = [float(np.mean([ev[i * n_l + j][0].elapsed_time(ev[i * n_l + j][1])
+                                    for i in range(steps)])) for j in range(n_l)]
+    return total_ms, launch_ms
+
+
+def e2e_case(case, steps, stream, dev):
+    """Same workload through the public API with host buffers: pinned host
+    inputs copied in, the call, the result copied out -- all timed."""
+    import torch
+    hx = [x.cpu().pin_memory() for x in case.x]
+    hwp = [w.cpu().pin_memory() for w in case.wp[0]]
+    hws = [w.cpu().pin_memory() for w in case.ws[0]]
+    hy = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for y in case.y]
+    dx = [torch.empty_like(x) for x in case.x]
+    dwp = [torch.empty_like(w) for w in case.wp[0]]
+    dws = [torch.empty_like(w) for w in case.ws[0]]
+    h2d = sum(t.nbytes for t in hx + hwp + hws)
+    d2h = sum(t.nbytes for t in hy)
+
+    def one():
+        with torch.cuda.stream(stream):
+            for j, t in enumerate(case.linears):
+                dx[j].copy_(hx[j], non_blocking=True)
+                dwp[j].copy_(hwp[j], non_blocking=True)
+                dws[j].copy_(hws[j], non_blocking=True)
+                case.lib.linear_ex(dx[j], dwp[j], dws[j], float(t.global_scale), case.flags,
+                                   out=case.y[j], stream=stream)
+                hy[j].copy_(case.y[j], non_blocking=True)
+
+    for _ in range(2):
+        one()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        one()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    return ms, h2d, d2h
+
+
+def run_ours(args):
+    import torch
+    from nvfp4_block_scaled_linear_gb300 import build as cuda_build
+
+    rank, world, local = dist_setup(args.gpus)
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    cuda_build.build()
+    from nvfp4_block_scaled_linear_gb300 import _lib as lib
+    lib.load_library()
+    hbm_peak, tc_peak, tc_sustained, peak_src = measured_peaks()
+    sampler = ClockSampler(dev.index if world == 1 else local)
+    sampler.start()
+    stream = torch.cuda.Stream(dev)
+
+    head = Case(args.workload, lib, dev)
+    total_ms, launch_ms = time_case(head, args.steps, args.warmup, stream, world, sampler)
+    step_s = total_ms / 1e3 / args.steps
+    max_step_s = aggregate_max(step_s, world)
+    tensor_bound = head.linears[0].M > 32
+    if tensor_bound:
+        value = whole_job_value(head.flops / 1e12, max_step_s, world)
+        unit = "TFLOP/s"
+    else:
+        value = whole_job_value(head.bytes / 1e9, max_step_s, world)
+        unit = "GB/s"
+
+    # dominant kernel = the longest launch of the step
+    j_dom = int(np.argmax(launch_ms))
+    t_dom = head.linears[j_dom]
+    from nvfp4_block_scaled_linear_gb300.inputs import algorithmic_bytes, flops
+    if tensor_bound:
+        achieved = flops(t_dom.M, t_dom.N, t_dom.K) / (launch_ms[j_dom] / 1e3) / 1e12
+        peak, runit, bound = tc_peak, "TFLOP/s", "tensor"
+    else:
+        achieved = algorithmic_bytes(t_dom.M, t_dom.N, t_dom.K, head.w.swiglu) / (
+            launch_ms[j_dom] / 1e3) / 1e9
+        peak, runit, bound = hbm_peak, "GB/s", "hbm"
+    roofline = {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": runit,
+                "frac": round(achieved / peak, 4), "peak_source": peak_src,
+                "kernel": head.kernel, "launch_us": round(launch_ms[j_dom] * 1e3, 3),
+                "traffic": profiled_traffic(head.kernel, head.name)}
+
+    line = {"metric": METRIC, "value": round(value, 2), "unit": unit, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(max_step_s * 1e3, 6), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded; checkpoint-schema layouts, random codes/scales/"
+                    "activations)",
+            "config": {"workload": head.name, "shapes": [[t.M, t.N, t.K] for t in head.linears],
+                       "swiglu": head.w.swiglu, "l2": head.l2_note(),
+                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "roofline": roofline, "gpu_launches": args.steps * head.launches_per_step}
+
+    if not args.no_extras:
+        e2e_ms, h2d, d2h = e2e_case(head, max(3, min(20, args.steps)), stream, dev)
+        e2e_val = (head.flops / 1e12 if tensor_bound else head.bytes / 1e9) / (e2e_ms / 1e3)
+        line["e2e"] = {"value": round(e2e_val * world, 2), "unit": unit,
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                       "ms_per_step": round(e2e_ms, 4)}
+        extras = {}
+        for name, steps in (("verify_down", 2000), ("layer_m32", 500), ("prefill", 10),
+                            ("prefill_swiglu", 10)):
+            if name == head.name:
+                continue
+            c = Case(name, lib, dev)
+            tot, lms = time_case(c, steps, 5, stream, world, sampler)
+            ms = tot / steps
+            ent = {"ms_per_step": round(ms, 5), "kernel": c.kernel,
+                   "launch_us": [round(v * 1e3, 2) for v in lms]}
+            if c.linears[0].M > 32:
+                tf = c.flops / (ms / 1e3) / 1e12
+                ent.update({"TFLOP/s": round(tf, 1), "frac_bf16_peak": round(tf / tc_peak, 4)})
+            else:
+                gb = c.bytes / (ms / 1e3) / 1e9
+                ent.update({"GB/s": round(gb, 1), "frac_hbm_peak": round(gb / hbm_peak, 4)})
+            extras[name] = ent
+            del c
+            torch.cuda.empty_cache()
+        line["workloads"] = extras
+        line["gpu_launches_extras"] = "not in the headline timed region"
+    sampler.stop()
+    line["clocks"] = sampler.summary()
+    if rank == 0 and not args.no_extras:
+        line["cpu_baseline"] = cpu_baseline(head, budget_s=args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------- CPU (oracle)
+def _oracle_step(t, rows, threads):
+    import oracle
+    return oracle.linear_f64(t.x_bits, t.w_packed[rows], t.w_scale[rows], t.global_scale,
+                             threads=threads)
+
+
+def cpu_baseline(case, budget_s=10.0):
+    """The oracle, as it stands, on the host cores: repeated passes over a
+    row sample of the headline workload for about budget_s seconds."""
+    import oracle
+    from nvfp4_block_scaled_linear_gb300.inputs import algorithmic_bytes
+    threads = oracle.default_threads()
+    t = case.linears[0]
+    # size one pass at ~1 s
+    rows = slice(0, min(t.N, 2048))
+    t0 = time.time()
+    _oracle_step(t, rows, threads)
+    one = time.time() - t0
+    n_rows = int(min(t.N, max(128, (rows.stop - rows.start) * 1.0 / max(one, 1e-3))))
+    rows = slice(0, n_rows)
+    done, t0 = 0, time.time()
+    while time.time() - t0 < budget_s:
+        _oracle_step(t, rows, threads)
+        done += 1
+    el = time.time() - t0
+    frac = n_rows / t.N
+    byts = (t.N * t.K // 2 + t.N * t.K // 16) * frac + 2 * t.M * t.K + 2 * t.M * n_rows
+    return {"value": round(byts * done / el / 1e9, 4), "unit": "GB/s", "cores": threads,
+            "kind": "oracle",
+            "sample": "%d passes over rows [0,%d) of %s (M=%d K=%d), %.1f s" % (
+                done, n_rows, case.name, t.M, t.K, el)}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    from nvfp4_block_scaled_linear_gb300.inputs import WORKLOADS, algorithmic_bytes, flops
+    w = WORKLOADS[args.workload]
+    t = w.draw()[0]
+    threads = oracle.default_threads()
+    # Size one step so that warmup + steps end within ~2 minutes.
+    probe_rows = min(t.N, 512)
+    t0 = time.time()
+    _oracle_step(t, slice(0, probe_rows), threads)
+    per_row = (time.time() - t0) / probe_rows
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    n_rows = int(max(1, min(t.N, budget / max(per_row, 1e-9))))
+    if t.M > 32:
+        # large-M: sample activation rows too
+        pass
+    rows = slice(0, n_rows)
+    for _ in range(args.warmup):
+        _oracle_step(t, rows, threads)
+    t0 = time.time()
+    for _ in range(args.steps):
+        _oracle_step(t, rows, threads)
+    el = time.time() - t0
+    frac = n_rows / t.N
+    tensor_bound = t.M > 32
+    if tensor_bound:
+        units = flops(t.M, n_rows, t.K) / 1e12
+        unit = "TFLOP/s"
+    else:
+        units = ((t.N * t.K // 2 + t.N * t.K // 16) * frac + 2 * t.M * t.K
+                 + 2 * t.M * n_rows) / 1e9
+        unit = "GB/s"
+    value = units * args.steps / el
+    sample = "rows [0,%d) of %d per step (M=%d K=%d)" % (n_rows, t.N, t.M, t.K)
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": unit,
+            "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded)",
+            "config": {"workload": w.name, "shapes": [[t.M, t.N, t.K]], "swiglu": w.swiglu},
+            "cpu_baseline": {"value": round(value, 6), "unit": unit, "cores": threads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 6), "unit": unit, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=HEADLINE)
+    ap.add_argument("--no-extras", action="store_true",
+                    help="headline only: no e2e, other workloads or CPU baseline")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,124 @@
+/*
+ * nvfp4_linear.h -- C ABI of libnvfp4_linear.so, the GB300 (sm_103a) NVFP4
+ * W4A16 block-scaled linear layer.
+ *
+ * Operation (FlashRT docs, "Qwen3.6-27B NVFP4 on RTX 5090", section 1 "Model
+ * dependencies", checkpoint condition 2 -- the compressed-tensors
+ * nvfp4-pack-quantized schema -- and the section 1 table, "NVFP4 W4A16"):
+ *
+ *   w[n,k] = e2m1(code[n,k]) * e4m3(w_scale[n, k/16]) / global_scale
+ *   y[m,n] = sum_k x[m,k] * w[n,k]          accumulated in fp32
+ *
+ * Arguments common to the compute entry points
+ *   x            device pointer, bf16 [M, K], row-major, contiguous.
+ *   w_packed     device pointer, uint8 [N, K/2]: FP4 e2m1 codes, two per
+ *                byte, the low nibble holding the even k.
+ *   w_scale      device pointer, uint8 [N, K/16]: fp8 e4m3 (E4M3FN) block
+ *                scales, one per 16 consecutive k of a row.
+ *   global_scale fp32 scalar; the weights are divided by it (it is the
+ *                checkpoint's "448 / amax").  Used as given.
+ *   y            device pointer, output, row-major, contiguous (shape and
+ *                type per entry point).  Must not overlap the inputs.
+ *   M, N, K      M >= 0 activation rows (M == 0 is a no-op; x and y may
+ *                then be NULL), N > 0 weight
+ *                rows with N % 128 == 0, K > 0 with K % 256 == 0.
+ *   stream       a cudaStream_t (0 = the legacy default stream).
+ *
+ * Ownership: every buffer belongs to the caller.  The library allocates no
+ * device or host memory per call and keeps no state besides per-device
+ * attributes it caches on first use (device properties, kernel attributes,
+ * the address of its device error word).
+ *
+ * Behaviour: calls are asynchronous on `stream`; they validate on the host,
+ * launch one kernel, and return without synchronising.  A rejected call
+ * launches nothing.  A device-side failure (a pipeline wait that timed out)
+ * does not fault the context: the kernel winds down and sets a bit in the
+ * library's device error word, readable with nvfp4_device_status().
+ *
+ * Status codes (return values): see NVFP4_* below; nvfp4_status_string()
+ * gives a message.
+ */
+#ifndef NVFP4_LINEAR_H
+#define NVFP4_LINEAR_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define NVFP4_ABI_VERSION 1
+
+#define NVFP4_OK 0
+#define NVFP4_ERR_INVALID (-1)      /* null pointer, negative/zero size, bad flags */
+#define NVFP4_ERR_MISALIGNED (-2)   /* a pointer is not 16-byte aligned */
+#define NVFP4_ERR_SHAPE (-3)        /* K % 256 != 0 or N % 128 != 0 */
+#define NVFP4_ERR_LAUNCH (-4)       /* the CUDA runtime refused the launch */
+#define NVFP4_ERR_DEVICE (-5)       /* no current device, or not an sm_103 GPU */
+
+/* Flags of nvfp4_linear_ex. */
+#define NVFP4_FLAG_SWIGLU 1u        /* fused gate/up: y = silu(gate) * up */
+#define NVFP4_FLAG_F32_OUT 2u       /* write fp32 (before bf16 rounding) */
+#define NVFP4_FLAG_FORCE_SMALLM 4u  /* force the few-row kernel (needs M <= 32) */
+#define NVFP4_FLAG_FORCE_TCGEMM 8u  /* force the tcgen05 tensor-core kernel */
+
+/* Kernel identifiers returned by nvfp4_linear_kernel_for. */
+#define NVFP4_KERNEL_NONE 0
+#define NVFP4_KERNEL_SMALLM 1       /* M <= 32: weight-streaming, register-fed MMA */
+#define NVFP4_KERNEL_TCGEMM 2       /* M > 32: tcgen05 / TMEM tensor-core GEMM */
+
+/* Version of this ABI (NVFP4_ABI_VERSION). */
+int nvfp4_abi_version(void);
+
+/* Static message for a status code. Never NULL. */
+const char* nvfp4_status_string(int status);
+
+/* y[M, N] bf16 = RNE_bf16(fp32 result).  The linear layer of the pages:
+ * MLP gate/up/down and full-attention q/k/v/o projections in decode,
+ * speculative verify and prefill. */
+int nvfp4_linear(const void* x, const uint8_t* w_packed, const uint8_t* w_scale,
+                 float global_scale, void* y, int64_t M, int64_t N, int64_t K,
+                 void* stream);
+
+/* y[M, N] fp32: the same result before the bf16 rounding (for checking the
+ * accumulator against an error bound). */
+int nvfp4_linear_f32(const void* x, const uint8_t* w_packed, const uint8_t* w_scale,
+                     float global_scale, float* y, int64_t M, int64_t N, int64_t K,
+                     void* stream);
+
+/* Fused MLP gate/up projection with SwiGLU epilogue (FlashRT docs section 4,
+ * fused gate/up GEMM; qwen36-fp4 README, SwiGLU kernel).  The weight holds
+ * gate rows [0, N/2) then up rows [N/2, N), one global scale for both;
+ * y[M, N/2] bf16 = silu(g) * u with g, u the fp32 results of the two halves
+ * and silu(g) = g / (1 + exp(-g)), computed in fp32. */
+int nvfp4_linear_swiglu(const void* x, const uint8_t* w_packed, const uint8_t* w_scale,
+                        float global_scale, void* y, int64_t M, int64_t N, int64_t K,
+                        void* stream);
+
+/* As nvfp4_linear_swiglu with fp32 output [M, N/2]. */
+int nvfp4_linear_swiglu_f32(const void* x, const uint8_t* w_packed,
+                            const uint8_t* w_scale, float global_scale, float* y,
+                            int64_t M, int64_t N, int64_t K, void* stream);
+
+/* General form of the four calls above; `flags` is an OR of NVFP4_FLAG_*.
+ * The FORCE flags pick a kernel regardless of M (for A/B measurements and
+ * for checking both kernels on the same inputs). */
+int nvfp4_linear_ex(const void* x, const uint8_t* w_packed, const uint8_t* w_scale,
+                    float global_scale, void* y, int64_t M, int64_t N, int64_t K,
+                    unsigned int flags, void* stream);
+
+/* Which kernel a call with these sizes and flags would launch
+ * (NVFP4_KERNEL_*), or NVFP4_KERNEL_NONE if the call would be rejected.
+ * Pure host function: touches no device. */
+int nvfp4_linear_kernel_for(int64_t M, int64_t N, int64_t K, unsigned int flags);
+
+/* Read the current device's error word (OR of bits set by kernels since it
+ * was last cleared: bit 0 = a pipeline wait timed out) into *bits; clear it
+ * if `clear` is non-zero.  Synchronises with the device.  Returns a status. */
+int nvfp4_device_status(unsigned int* bits, int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4_LINEAR_H */

@@ -1,0 +1,174 @@
+"""ctypes binding of libnvfp4_linear.so (include/nvfp4_linear.h).
+
+Argument marshalling only: shape/dtype/device checks, output allocation with
+torch, the current CUDA stream, and the call.  Every step of the layer runs
+in the library's kernels; there is no CPU or PyTorch fallback, and a missing
+library or GPU raises.
+"""
+import ctypes
+import os
+import re
+
+import torch
+
+from . import build as _build
+
+# Mirrors of the header's constants.
+OK = 0
+FLAG_SWIGLU = 1
+FLAG_F32_OUT = 2
+FLAG_FORCE_SMALLM = 4
+FLAG_FORCE_TCGEMM = 8
+KERNEL_NONE, KERNEL_SMALLM, KERNEL_TCGEMM = 0, 1, 2
+KERNEL_NAMES = {KERNEL_SMALLM: "smallm", KERNEL_TCGEMM: "tcgemm"}
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                      "include", "nvfp4_linear.h")
+
+_lib = None
+
+
+class Nvfp4Error(RuntimeError):
+    def __init__(self, status, what=""):
+        self.status = status
+        msg = library().nvfp4_status_string(status).decode() if _lib else str(status)
+        super().__init__("%s failed: %s (status %d)" % (what or "nvfp4", msg, status))
+
+
+def header_functions():
+    """Names of the functions declared in include/nvfp4_linear.h."""
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\*?(nvfp4_\w+)\s*\(",
+                                 text, re.M)))
+
+
+def load_library(path=None):
+    """Load the built library (never builds it; __graft_entry__.build() or
+    ``python -m nvfp4_block_scaled_linear_gb300.build`` does)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or _build.LIB
+    if not os.path.exists(path):
+        raise RuntimeError("libnvfp4_linear.so is not built (%s); run "
+                           "python -m nvfp4_block_scaled_linear_gb300.build" % path)
+    lib = ctypes.CDLL(path)
+    P, i64, u32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint
+    lib.nvfp4_abi_version.restype = ctypes.c_int
+    lib.nvfp4_abi_version.argtypes = []
+    lib.nvfp4_status_string.restype = ctypes.c_char_p
+    lib.nvfp4_status_string.argtypes = [ctypes.c_int]
+    for name in ("nvfp4_linear", "nvfp4_linear_f32", "nvfp4_linear_swiglu",
+                 "nvfp4_linear_swiglu_f32"):
+        f = getattr(lib, name)
+        f.restype = ctypes.c_int
+        f.argtypes = [P, P, P, ctypes.c_float, P, i64, i64, i64, P]
+    lib.nvfp4_linear_ex.restype = ctypes.c_int
+    lib.nvfp4_linear_ex.argtypes = [P, P, P, ctypes.c_float, P, i64, i64, i64, u32, P]
+    lib.nvfp4_linear_kernel_for.restype = ctypes.c_int
+    lib.nvfp4_linear_kernel_for.argtypes = [i64, i64, i64, u32]
+    lib.nvfp4_device_status.restype = ctypes.c_int
+    lib.nvfp4_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), ctypes.c_int]
+    _lib = lib
+    return lib
+
+
+def library():
+    return load_library()
+
+
+def abi_version() -> int:
+    return library().nvfp4_abi_version()
+
+
+def status_string(status: int) -> str:
+    return library().nvfp4_status_string(int(status)).decode()
+
+
+def kernel_for(M, N, K, flags=0) -> int:
+    return library().nvfp4_linear_kernel_for(int(M), int(N), int(K), int(flags))
+
+
+def device_error(clear: bool = True) -> int:
+    """The device error word (bit 0: a pipeline wait timed out); synchronises."""
+    bits = ctypes.c_uint(0)
+    st = library().nvfp4_device_status(ctypes.byref(bits), 1 if clear else 0)
+    if st != OK:
+        raise Nvfp4Error(st, "nvfp4_device_status")
+    return bits.value
+
+
+def _as_u8(t, name):
+    if t.dtype == torch.uint8:
+        return t
+    if t.dtype in (torch.int8, torch.float8_e4m3fn):
+        return t.view(torch.uint8)
+    raise TypeError("%s must be uint8 (or float8_e4m3fn for scales), got %s" % (name, t.dtype))
+
+
+def _check(x, w_packed, w_scale):
+    if not (x.is_cuda and w_packed.is_cuda and w_scale.is_cuda):
+        raise ValueError("x, w_packed and w_scale must be CUDA tensors")
+    if x.dtype != torch.bfloat16:
+        raise TypeError("x must be bfloat16, got %s" % x.dtype)
+    w_packed = _as_u8(w_packed, "w_packed")
+    w_scale = _as_u8(w_scale, "w_scale")
+    if x.dim() != 2 or w_packed.dim() != 2 or w_scale.dim() != 2:
+        raise ValueError("x, w_packed and w_scale must be 2-D")
+    M, K = x.shape
+    N = w_packed.shape[0]
+    if tuple(w_packed.shape) != (N, K // 2) or tuple(w_scale.shape) != (N, K // 16):
+        raise ValueError("shapes disagree: x %s, w_packed %s, w_scale %s"
+                         % (tuple(x.shape), tuple(w_packed.shape), tuple(w_scale.shape)))
+    if not (x.is_contiguous() and w_packed.is_contiguous() and w_scale.is_contiguous()):
+        raise ValueError("x, w_packed and w_scale must be contiguous")
+    if len({x.device, w_packed.device, w_scale.device}) != 1:
+        raise ValueError("inputs live on different devices")
+    return w_packed, w_scale, M, N, K
+
+
+def linear_ex(x, w_packed, w_scale, global_scale, flags=0, out=None, stream=None):
+    """Call nvfp4_linear_ex; allocate ``out`` if not given and return it."""
+    w_packed, w_scale, M, N, K = _check(x, w_packed, w_scale)
+    n_out = N // 2 if flags & FLAG_SWIGLU else N
+    dtype = torch.float32 if flags & FLAG_F32_OUT else torch.bfloat16
+    if out is None:
+        out = torch.empty((M, n_out), dtype=dtype, device=x.device)
+    elif (out.dtype != dtype or tuple(out.shape) != (M, n_out) or not out.is_contiguous()
+          or out.device != x.device):
+        raise ValueError("out must be a contiguous %s tensor of shape %s on %s"
+                         % (dtype, (M, n_out), x.device))
+    if stream is None:
+        stream = torch.cuda.current_stream(x.device)
+    with torch.cuda.device(x.device):
+        st = library().nvfp4_linear_ex(x.data_ptr(), w_packed.data_ptr(), w_scale.data_ptr(),
+                                       float(global_scale), out.data_ptr(), M, N, K,
+                                       int(flags), ctypes.c_void_p(stream.cuda_stream))
+    if st != OK:
+        raise Nvfp4Error(st, "nvfp4_linear_ex")
+    return out
+
+
+def linear(x, w_packed, w_scale, global_scale, out=None, stream=None):
+    """y[M, N] bf16 = x[M, K] . W^T with W the dequantised NVFP4 weight."""
+    return linear_ex(x, w_packed, w_scale, global_scale, 0, out, stream)
+
+
+def linear_f32(x, w_packed, w_scale, global_scale, out=None, stream=None):
+    """Same as ``linear`` with fp32 output (before the bf16 rounding)."""
+    return linear_ex(x, w_packed, w_scale, global_scale, FLAG_F32_OUT, out, stream)
+
+
+def linear_swiglu(x, w_packed, w_scale, global_scale, out=None, stream=None):
+    """Fused gate/up: y[M, N/2] bf16 = silu(x W_gate^T) * (x W_up^T)."""
+    return linear_ex(x, w_packed, w_scale, global_scale, FLAG_SWIGLU, out, stream)
+
+
+def linear_swiglu_f32(x, w_packed, w_scale, global_scale, out=None, stream=None):
+    return linear_ex(x, w_packed, w_scale, global_scale, FLAG_SWIGLU | FLAG_F32_OUT, out,
+                     stream)
+
+
+def choose_plan(M, N, K, flags=0):
+    """Name of the kernel a call would launch ('smallm' / 'tcgemm'), or None."""
+    return KERNEL_NAMES.get(kernel_for(M, N, K, flags))

@@ -1,0 +1,73 @@
+// dequant.cuh -- e2m1 x e4m3 block dequantisation in registers.
+//
+// Format (FlashRT docs, "Qwen3.6-27B NVFP4 on RTX 5090", section 1, checkpoint
+// condition 2): weight_packed u8 (out, in/2) holds FP4 e2m1 codes two per
+// byte (low nibble = even k), weight_scale holds one fp8 e4m3 per 16 inputs.
+//
+// A code times a block scale has at most 2 x 4 significant bits, so the
+// product is exact in bf16.  The kernels therefore feed exact bf16 weights
+// to the tensor cores and apply the fp32 global scale once, in the epilogue.
+//
+// Bit trick.  Placing a code's three magnitude bits (e1 e0 m) at bf16 bits
+// 8..6 and its sign at bit 15 gives the bf16 number code * 2^-126: the two
+// exponent bits land in the low end of the bf16 exponent field, the mantissa
+// bit at the top of the mantissa, and exponent 0 (the e2m1 subnormals 0 and
+// 0.5) lands on bf16's own subnormals.  One bf16 multiply by
+// S = scale * 2^116 then yields code * scale * 2^-10 exactly (2^-20 at the
+// smallest, so never subnormal); the epilogue multiplies by 2^10.
+#pragma once
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace nvfp4 {
+
+// Exponent offset folded into the dequantised weights; undone in the epilogue.
+constexpr float kWeightPow2 = 1024.0f;   // 2^10
+
+// bf16x2 (S, S) for an e4m3 bit pattern, S = value * 2^116; NaN for S.1111.111.
+// Exact: an e4m3 value has at most 4 significant bits.
+__device__ __forceinline__ uint32_t scale_pair_from_e4m3(uint32_t b) {
+  const uint32_t e = (b >> 3) & 15u, m = b & 7u;
+  uint32_t f32;
+  if (e == 15u && m == 7u) {
+    f32 = 0x7FC00000u;                                  // NaN
+  } else if (e != 0u) {
+    // 2^(e-7) * (1 + m/8) * 2^116 : biased exponent e - 7 + 116 + 127
+    f32 = ((e + 236u) << 23) | (m << 20);
+  } else {
+    // subnormal: (m/8) * 2^-6 * 2^116 = m * 2^107
+    f32 = __float_as_uint(static_cast<float>(m) * 0x1p107f);
+  }
+  f32 |= (b & 0x80u) << 24;                             // sign
+  const uint32_t h = f32 >> 16;                         // exact bf16
+  return h | (h << 16);
+}
+
+// Eight codes (one 32-bit word, k = 0..7 in nibble order) times the pair
+// scale S -> four bf16x2 words pairing (k, k+4):
+//   out[i] = ( w(k=i), w(k=i+4) ),  i = 0..3,
+// each w = code * scale * 2^-10.  Callers that need consecutive k use
+// pair_consecutive() below.
+__device__ __forceinline__ void dequant8_strided(uint32_t w, uint32_t S, uint32_t* out) {
+  const uint32_t kMag = 0x01C001C0u, kSign = 0x80008000u;
+  const uint32_t r0 = ((w << 6) & kMag) | ((w << 12) & kSign);
+  const uint32_t r1 = ((w << 2) & kMag) | ((w << 8) & kSign);
+  const uint32_t r2 = ((w >> 2) & kMag) | ((w << 4) & kSign);
+  const uint32_t r3 = ((w >> 6) & kMag) | (w & kSign);
+  out[0] = bf16x2_mul(r0, S);
+  out[1] = bf16x2_mul(r1, S);
+  out[2] = bf16x2_mul(r2, S);
+  out[3] = bf16x2_mul(r3, S);
+}
+
+// Reorder the (k, k+4) pairs of dequant8_strided into consecutive pairs
+// (0,1) (2,3) (4,5) (6,7), the order of a row in memory.
+__device__ __forceinline__ void pair_consecutive(const uint32_t* p, uint32_t* out) {
+  out[0] = prmt(p[0], p[1], 0x5410u);   // k0 | k1
+  out[1] = prmt(p[2], p[3], 0x5410u);   // k2 | k3
+  out[2] = prmt(p[0], p[1], 0x7632u);   // k4 | k5
+  out[3] = prmt(p[2], p[3], 0x7632u);   // k6 | k7
+}
+
+}  // namespace nvfp4

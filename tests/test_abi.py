@@ -1,0 +1,95 @@
+"""The C ABI on the host: the library builds, loads, exports every function
+include/nvfp4_linear.h declares, and rejects bad arguments before touching a
+device.  No call here reaches a kernel (none of them gets past validation)."""
+import ctypes
+
+import pytest
+import torch
+
+from nvfp4_block_scaled_linear_gb300 import _lib
+from nvfp4_block_scaled_linear_gb300 import build as cuda_build
+
+
+@pytest.fixture(scope="module")
+def lib():
+    cuda_build.build()
+    return _lib.load_library()
+
+
+def test_exports_every_declared_function(lib):
+    names = _lib.header_functions()
+    assert len(names) >= 9, names
+    for n in names:
+        assert hasattr(lib, n), "missing export " + n
+
+
+def test_header_constants_match_binding():
+    text = open(_lib.HEADER).read()
+    for name, value in (("NVFP4_FLAG_SWIGLU", _lib.FLAG_SWIGLU),
+                        ("NVFP4_FLAG_F32_OUT", _lib.FLAG_F32_OUT),
+                        ("NVFP4_FLAG_FORCE_SMALLM", _lib.FLAG_FORCE_SMALLM),
+                        ("NVFP4_FLAG_FORCE_TCGEMM", _lib.FLAG_FORCE_TCGEMM),
+                        ("NVFP4_KERNEL_SMALLM", _lib.KERNEL_SMALLM),
+                        ("NVFP4_KERNEL_TCGEMM", _lib.KERNEL_TCGEMM)):
+        assert "#define %s %du" % (name, value) in text or "#define %s %d " % (name, value) in text
+
+
+def test_version_and_status_strings(lib):
+    assert _lib.abi_version() == 1
+    for st in (0, -1, -2, -3, -4, -5, 7):
+        s = _lib.status_string(st)
+        assert isinstance(s, str) and s
+
+
+@pytest.mark.parametrize("M,N,K,flags,expect", [
+    (1, 256, 512, 0, _lib.KERNEL_SMALLM),
+    (32, 34816, 5120, 0, _lib.KERNEL_SMALLM),
+    (33, 34816, 5120, 0, _lib.KERNEL_TCGEMM),
+    (8192, 34816, 5120, _lib.FLAG_SWIGLU, _lib.KERNEL_TCGEMM),
+    (7, 5120, 17408, _lib.FLAG_FORCE_TCGEMM, _lib.KERNEL_TCGEMM),
+    (64, 256, 512, _lib.FLAG_FORCE_SMALLM, _lib.KERNEL_NONE),   # smallm needs M <= 32
+    (1, 256, 500, 0, _lib.KERNEL_NONE),                          # K % 256
+    (1, 200, 512, 0, _lib.KERNEL_NONE),                          # N % 128
+    (0, 256, 512, 0, _lib.KERNEL_NONE),                          # empty: nothing launched
+    (-1, 256, 512, 0, _lib.KERNEL_NONE),
+    (1, 256, 512, 64, _lib.KERNEL_NONE),                         # unknown flag
+    (1, 256, 512, _lib.FLAG_FORCE_SMALLM | _lib.FLAG_FORCE_TCGEMM, _lib.KERNEL_NONE),
+])
+def test_kernel_choice(lib, M, N, K, flags, expect):
+    assert _lib.kernel_for(M, N, K, flags) == expect
+
+
+def _call(lib, x, wp, ws, y, M, N, K):
+    return lib.nvfp4_linear(x, wp, ws, ctypes.c_float(1.0), y, M, N, K, None)
+
+
+def test_rejects_before_any_device_work(lib):
+    A = 0x10000           # fake, 16-byte aligned, never dereferenced
+    assert _call(lib, None, A, A, A, 1, 256, 512) == -1
+    assert _call(lib, A, None, A, A, 1, 256, 512) == -1
+    assert _call(lib, A, A, None, A, 1, 256, 512) == -1
+    assert _call(lib, A, A, A, None, 1, 256, 512) == -1
+    assert _call(lib, A, A, A, A, -1, 256, 512) == -1
+    assert _call(lib, A, A, A, A, 1, 0, 512) == -1
+    assert _call(lib, A, A, A, A, 1, 256, 0) == -1
+    assert _call(lib, A + 2, A, A, A, 1, 256, 512) == -2
+    assert _call(lib, A, A + 8, A, A, 1, 256, 512) == -2
+    assert _call(lib, A, A, A, A + 4, 1, 256, 512) == -2
+    assert _call(lib, A, A, A, A, 1, 256, 384) == -3
+    assert _call(lib, A, A, A, A, 1, 192, 512) == -3
+    assert lib.nvfp4_linear_ex(A, A, A, ctypes.c_float(1.0), A, 1, 256, 512, 1 << 7, None) == -1
+    assert lib.nvfp4_linear_ex(A, A, A, ctypes.c_float(1.0), A, 40, 256, 512,
+                               _lib.FLAG_FORCE_SMALLM, None) == -1
+    # M == 0 is a valid empty call: nothing to do, nothing launched; x and y
+    # may be NULL (an empty tensor's data pointer)
+    assert _call(lib, A, A, A, A, 0, 256, 512) == 0
+    assert _call(lib, None, A, A, None, 0, 256, 512) == 0
+    assert _call(lib, None, None, A, None, 0, 256, 512) == -1
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    x = torch.zeros(1, 512, dtype=torch.bfloat16)
+    wp = torch.zeros(256, 256, dtype=torch.uint8)
+    ws = torch.zeros(256, 32, dtype=torch.uint8)
+    with pytest.raises(ValueError):
+        _lib.linear(x, wp, ws, 1.0)

@@ -1,0 +1,271 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle, element
+by element, on seeded inputs.  Tolerances are documented in _parity.py."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from _parity import (check_bf16, check_f32, check_swiglu_bf16, check_swiglu_f32)
+from nvfp4_block_scaled_linear_gb300 import _lib
+from nvfp4_block_scaled_linear_gb300 import build as cuda_build
+from nvfp4_block_scaled_linear_gb300.inputs import (WORKLOADS, LinearInputs, make_linear)
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    cuda_build.build()
+    _lib.load_library()
+    _lib.device_error(clear=True)
+    yield
+    assert _lib.device_error(clear=True) == 0, "a kernel reported a wait timeout"
+
+
+def to_dev(t: LinearInputs):
+    x = torch.from_numpy(t.x_bits.view(np.int16)).view(torch.bfloat16).to(DEV)
+    return x, torch.from_numpy(t.w_packed).to(DEV), torch.from_numpy(t.w_scale).to(DEV)
+
+
+def bf16_bits(y):
+    return y.cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def run(t, flags=0):
+    x, wp, ws = to_dev(t)
+    y = _lib.linear_ex(x, wp, ws, float(t.global_scale), flags)
+    torch.cuda.synchronize()
+    return y
+
+
+def full_check(t, flags=0, what=""):
+    y64, a = oracle.linear_f64(t.x_bits, t.w_packed, t.w_scale, t.global_scale)
+    if flags & _lib.FLAG_SWIGLU:
+        out64 = oracle.swiglu_f64(y64)
+        y32 = run(t, flags | _lib.FLAG_F32_OUT).cpu().numpy()
+        check_swiglu_f32(y32, y64, a, out64, what + " f32")
+        ybf = bf16_bits(run(t, flags))
+        return check_swiglu_bf16(ybf, y64, a, out64, oracle.to_bf16_bits(out64), what + " bf16")
+    y32 = run(t, flags | _lib.FLAG_F32_OUT).cpu().numpy()
+    check_f32(y32, y64, a, what + " f32")
+    ybf = bf16_bits(run(t, flags))
+    strict, _ = check_bf16(ybf, y64, a, oracle.to_bf16_bits(y64), what + " bf16")
+    return strict
+
+
+# ------------------------------------------------------------------ small M
+@pytest.mark.parametrize("M", [1, 2, 5, 7, 8, 9, 16, 17, 24, 25, 31, 32])
+def test_smallm_all_row_counts(M):
+    t = make_linear(M, 384, 1024, seed=100 + M)
+    assert _lib.kernel_for(M, 384, 1024) == _lib.KERNEL_SMALLM
+    full_check(t, what="smallm M=%d" % M)
+
+
+@pytest.mark.parametrize("N,K", [(128, 256), (256, 768), (640, 4352), (1024, 2304)])
+def test_smallm_shapes_and_uneven_splits(N, K):
+    # K/256 stages split over clusters of up to 8 CTAs, unevenly when they
+    # do not divide
+    t = make_linear(7, N, K, seed=N + K)
+    full_check(t, what="smallm N=%d K=%d" % (N, K))
+
+
+@pytest.mark.parametrize("M", [1, 7, 32])
+def test_smallm_swiglu(M):
+    t = make_linear(M, 512, 1024, seed=300 + M)
+    full_check(t, _lib.FLAG_SWIGLU, what="smallm swiglu M=%d" % M)
+
+
+# ------------------------------------------------------------------ tcgen05
+@pytest.mark.parametrize("M", [33, 64, 255, 256, 257, 600])
+def test_tcgemm_row_counts_and_tails(M):
+    t = make_linear(M, 384, 1024, seed=200 + M, big_row_frac=0.02)
+    assert _lib.kernel_for(M, 384, 1024) == _lib.KERNEL_TCGEMM
+    full_check(t, what="tcgemm M=%d" % M)
+
+
+@pytest.mark.parametrize("N,K", [(128, 256), (256, 4096), (640, 512)])
+def test_tcgemm_shapes(N, K):
+    t = make_linear(100, N, K, seed=N * 7 + K)
+    full_check(t, what="tcgemm N=%d K=%d" % (N, K))
+
+
+@pytest.mark.parametrize("M", [40, 300])
+def test_tcgemm_swiglu(M):
+    t = make_linear(M, 512, 1024, seed=400 + M)
+    full_check(t, _lib.FLAG_SWIGLU, what="tcgemm swiglu M=%d" % M)
+
+
+@pytest.mark.parametrize("M", [1, 7, 32])
+def test_both_kernels_agree_at_small_m(M):
+    t = make_linear(M, 256, 512, seed=500 + M)
+    full_check(t, _lib.FLAG_FORCE_TCGEMM, what="forced tcgemm M=%d" % M)
+    full_check(t, _lib.FLAG_FORCE_SMALLM, what="forced smallm M=%d" % M)
+
+
+# ------------------------------------------------------------------ exactness
+def _exhaustive_products():
+    """Rows n = every e4m3 scale byte; inputs k = 0..15 carry codes 0..15;
+    x row m is one-hot at k = m, so y[m, n] = code(m) * scale(n) / gs: one
+    exact product per output, which must match bit for bit."""
+    N, K, M = 256, 256, 16
+    wp = np.zeros((N, K // 2), np.uint8)
+    codes = np.arange(K) % 16
+    wp[:] = (codes[0::2] | (codes[1::2] << 4)).astype(np.uint8)
+    ws = np.repeat(np.arange(256, dtype=np.uint8)[:, None], K // 16, axis=1)
+    x = np.zeros((M, K), np.uint16)
+    x[np.arange(M), np.arange(M)] = 0x3F80
+    return LinearInputs(x, wp, ws, np.float32(1.0))
+
+
+@pytest.mark.parametrize("flags", [_lib.FLAG_FORCE_SMALLM, _lib.FLAG_FORCE_TCGEMM])
+def test_every_code_times_every_scale_is_exact(flags):
+    t = _exhaustive_products()
+    y64, _ = oracle.linear_f64(t.x_bits, t.w_packed, t.w_scale, t.global_scale)
+    y32 = run(t, flags | _lib.FLAG_F32_OUT).cpu().numpy().astype(np.float64)
+    nan = np.isnan(y64)
+    assert np.array_equal(np.isnan(y32), nan)
+    assert np.array_equal(y32[~nan], y64[~nan])
+
+
+@pytest.mark.parametrize("M,flags", [(5, 0), (70, 0), (5, _lib.FLAG_FORCE_TCGEMM)])
+def test_exact_integer_inputs_are_bit_exact(M, flags):
+    # small-integer activations, power-of-two scales, global scale 1: every
+    # partial sum is an exactly representable fp32 number, so the result is
+    # exact whatever the summation order
+    rng = np.random.default_rng(9)
+    N, K = 256, 1024
+    xs = rng.integers(-3, 4, size=(M, K)).astype(np.float32)
+    x = torch.from_numpy(xs).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    wp = rng.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    ws = rng.choice(np.array([0x30, 0x38, 0x40, 0x48], np.uint8), size=(N, K // 16))
+    t = LinearInputs(x, wp, ws, np.float32(1.0))
+    y64, _ = oracle.linear_f64(t.x_bits, t.w_packed, t.w_scale, t.global_scale)
+    y32 = run(t, flags | _lib.FLAG_F32_OUT).cpu().numpy().astype(np.float64)
+    assert np.array_equal(y32, y64)
+
+
+@pytest.mark.parametrize("M", [3, 50])
+def test_sign_flip_negates_exactly(M):
+    t = make_linear(M, 256, 512, seed=600 + M)
+    y = run(t, _lib.FLAG_F32_OUT).cpu().numpy()
+    flipped = LinearInputs(t.x_bits, t.w_packed ^ np.uint8(0x88), t.w_scale, t.global_scale)
+    y_neg = run(flipped, _lib.FLAG_F32_OUT).cpu().numpy()
+    assert np.array_equal(y_neg, -y)
+
+
+@pytest.mark.parametrize("M", [1, 40])
+def test_nibble_order(M):
+    K, N = 256, 128
+    x = np.zeros((M, K), np.uint16)
+    x[:, 0] = 0x3F80          # 1.0 at k = 0
+    x[:, 1] = 0x4000          # 2.0 at k = 1
+    ws = np.full((N, K // 16), 0x38, np.uint8)
+    lo = np.zeros((N, K // 2), np.uint8)
+    lo[:, 0] = 0x07           # 6.0 at k = 0 (low nibble)
+    hi = np.zeros((N, K // 2), np.uint8)
+    hi[:, 0] = 0x70           # 6.0 at k = 1 (high nibble)
+    y_lo = run(LinearInputs(x, lo, ws, np.float32(1.0)), _lib.FLAG_F32_OUT).cpu().numpy()
+    y_hi = run(LinearInputs(x, hi, ws, np.float32(1.0)), _lib.FLAG_F32_OUT).cpu().numpy()
+    assert np.all(y_lo == 6.0) and np.all(y_hi == 12.0)
+
+
+def test_row_batch_invariance_verify_vs_decode():
+    # greedy decode (M = 1) and speculative verify (M = 7) see the same rows:
+    # each verify row must equal the single-row call on that row, bit for bit
+    t = make_linear(7, 1024, 2048, seed=700)
+    y7 = bf16_bits(run(t))
+    for i in range(7):
+        ti = LinearInputs(t.x_bits[i:i + 1].copy(), t.w_packed, t.w_scale, t.global_scale)
+        assert np.array_equal(bf16_bits(run(ti))[0], y7[i]), "row %d" % i
+
+
+# ------------------------------------------------------------------ edges
+def test_empty_m_is_a_no_op():
+    x = torch.zeros((0, 512), dtype=torch.bfloat16, device=DEV)
+    wp = torch.zeros((256, 256), dtype=torch.uint8, device=DEV)
+    ws = torch.zeros((256, 32), dtype=torch.uint8, device=DEV)
+    y = _lib.linear(x, wp, ws, 1.0)
+    assert tuple(y.shape) == (0, 256)
+
+
+def test_errors_on_device_buffers():
+    x = torch.zeros((1, 512 + 8), dtype=torch.bfloat16, device=DEV)
+    wp = torch.zeros((256, 256), dtype=torch.uint8, device=DEV)
+    ws = torch.zeros((256, 32), dtype=torch.uint8, device=DEV)
+    lib = _lib.library()
+    y = torch.empty((1, 256), dtype=torch.bfloat16, device=DEV)
+    s = torch.cuda.current_stream().cuda_stream
+    import ctypes
+    # x starting 2 bytes into an allocation: misaligned
+    st = lib.nvfp4_linear(x.data_ptr() + 2, wp.data_ptr(), ws.data_ptr(), ctypes.c_float(1.0),
+                          y.data_ptr(), 1, 256, 512, ctypes.c_void_p(s))
+    assert st == -2
+    st = lib.nvfp4_linear(x.data_ptr(), wp.data_ptr(), ws.data_ptr(), ctypes.c_float(1.0),
+                          y.data_ptr(), 1, 256, 520, ctypes.c_void_p(s))
+    assert st == -3
+
+
+@pytest.mark.parametrize("M", [3, 45])
+def test_output_guard_rows_untouched(M):
+    t = make_linear(M, 256, 512, seed=800 + M)
+    x, wp, ws = to_dev(t)
+    big = torch.full((M + 2, 256), 12345.0, dtype=torch.float32, device=DEV)
+    out = big[1:M + 1]
+    _lib.linear_f32(x, wp, ws, float(t.global_scale), out=out)
+    torch.cuda.synchronize()
+    assert torch.all(big[0] == 12345.0) and torch.all(big[M + 1] == 12345.0)
+
+
+def test_repeated_calls_are_deterministic():
+    t = make_linear(7, 512, 4096, seed=900)
+    a = bf16_bits(run(t))
+    for _ in range(3):
+        assert np.array_equal(bf16_bits(run(t)), a)
+
+
+# ------------------------------------------------------------------ full size
+def _sample_points(M, N, count, rng, big_rows=()):
+    m = rng.integers(0, M, count)
+    n = rng.integers(0, N, count)
+    extra_m = np.concatenate([np.array([0, M - 1], np.int64), np.asarray(big_rows, np.int64)[:8]])
+    extra_n = rng.integers(0, N, extra_m.size)
+    return np.concatenate([m, extra_m]), np.concatenate([n, extra_n])
+
+
+@pytest.mark.parametrize("name", ["decode_gate_up", "verify_down", "layer_m32", "prefill",
+                                  "prefill_swiglu"])
+def test_full_size_workloads_sampled(name):
+    """The benchmarked shapes, in the benchmark's launch configuration
+    (the same entry points and plan), checked at sampled outputs."""
+    w = WORKLOADS[name]
+    rng = np.random.default_rng(1234)
+    for t in w.draw():
+        x, wp, ws = to_dev(t)
+        flags = _lib.FLAG_SWIGLU if w.swiglu else 0
+        y32 = _lib.linear_ex(x, wp, ws, float(t.global_scale), flags | _lib.FLAG_F32_OUT)
+        ybf = _lib.linear_ex(x, wp, ws, float(t.global_scale), flags)
+        torch.cuda.synchronize()
+        n_out = y32.shape[1]
+        mi, ni = _sample_points(t.M, n_out, 1500 if t.M > 1 else 600, rng, t.big_rows)
+        y32s = y32.cpu().numpy()[mi, ni].astype(np.float64)
+        ybs = bf16_bits(ybf)[mi, ni]
+        if w.swiglu:
+            H = t.N // 2
+            g64, ga = oracle.linear_points_f64(t.x_bits, t.w_packed, t.w_scale, t.global_scale,
+                                               mi, ni)
+            u64, ua = oracle.linear_points_f64(t.x_bits, t.w_packed, t.w_scale, t.global_scale,
+                                               mi, ni + H)
+            y64 = np.stack([g64, u64], 1)
+            a = np.stack([ga, ua], 1)
+            out64 = oracle.swiglu_f64(y64)[:, 0]
+            check_swiglu_f32(y32s[:, None], y64, a, out64[:, None], name)
+            check_swiglu_bf16(ybs[:, None], y64, a, out64[:, None],
+                              oracle.to_bf16_bits(out64)[:, None], name)
+        else:
+            y64, a = oracle.linear_points_f64(t.x_bits, t.w_packed, t.w_scale, t.global_scale,
+                                              mi, ni)
+            check_f32(y32s, y64, a, "%s/%s" % (name, t.name))
+            check_bf16(ybs, y64, a, oracle.to_bf16_bits(y64), "%s/%s" % (name, t.name))
+        del x, wp, ws, y32, ybf
+        torch.cuda.empty_cache()
