@@ -7,8 +7,9 @@
 Prints ONE JSON line.  A step is one pass of the layer over one batch of the
 headline workload (decode GEMV over the fused MLP gate+up projection:
 M=1, K=5120, N=34816); ``value`` is algorithmic bytes per step / time per
-step (GB/s), inputs resident in HBM, K steps timed with CUDA events between
-barriers + device synchronisations.  Weights are rotated over enough copies
+step (GB/s), inputs resident in HBM, K steps replayed from CUDA graphs and
+timed with CUDA events on the launching stream, between barriers + device
+synchronisations (--eager: eager launches instead).  Weights are rotated over enough copies
 that the rotated set exceeds twice the L2 cache, so every step streams its
 weights from HBM.
 
@@ -184,14 +185,14 @@ def whole_job_value(units_per_rank, max_seconds, world):
 class Case:
     """Device-resident inputs of one workload, with rotated weight copies."""
 
-    def __init__(self, name, lib, dev, min_rotated_bytes=2 * L2_BYTES):
+    def __init__(self, name, lib, dev, min_rotated_bytes=2 * L2_BYTES, max_rows=None):
         import torch
         from nvfp4_block_scaled_linear_gb300.inputs import WORKLOADS, algorithmic_bytes, flops
         self.w = WORKLOADS[name]
         self.name = name
         self.lib = lib
         self.flags = lib.FLAG_SWIGLU if self.w.swiglu else 0
-        self.linears = self.w.draw()
+        self.linears = self.w.draw(max_rows)
         self.bytes = sum(algorithmic_bytes(t.M, t.N, t.K, self.w.swiglu) for t in self.linears)
         self.flops = sum(flops(t.M, t.N, t.K) for t in self.linears)
         per_copy = sum(t.w_packed.nbytes + t.w_scale.nbytes for t in self.linears)
@@ -209,18 +210,19 @@ class Case:
                   for t, n in zip(self.linears, n_out)]
         self.rotated_bytes = self.copies * per_copy + act
         self.launches_per_step = len(self.linears)
+        self.only = None          # restrict a step to one linear (per-linear timing)
         self.kernel = lib.choose_plan(self.linears[0].M, self.linears[0].N, self.linears[0].K,
                                       self.flags)
 
-    def step(self, i, stream, events=None):
+    def indices(self):
+        return range(len(self.linears)) if self.only is None else (self.only,)
+
+    def step(self, i, stream):
         c = i % self.copies
-        for j, t in enumerate(self.linears):
-            if events is not None:
-                events[0].record(stream)
+        for j in self.indices():
+            t = self.linears[j]
             self.lib.linear_ex(self.x[j], self.wp[c][j], self.ws[c][j], float(t.global_scale),
                                self.flags, out=self.y[j], stream=stream)
-            if events is not None:
-                events[1].record(stream)
 
     def l2_note(self):
         if self.copies > 1:
@@ -229,14 +231,83 @@ class Case:
         return "inputs larger than L2 (%d MB)" % (self.rotated_bytes >> 20)
 
 
-def time_case(case, steps, warmup, stream, world, sampler=None, per_launch=True):
+def _capture(case, n_steps, stream):
+    """A CUDA graph of n_steps consecutive steps (weight copies rotating from
+    copy 0), captured on `stream`."""
     import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(n_steps):
+                case.step(i, stream)
+    return g
+
+
+def _replay_steps(stream, steps, chunk_graph, chunk, tail_graph):
+    import torch
+    with torch.cuda.stream(stream):
+        for _ in range(steps // chunk):
+            chunk_graph.replay()
+        if tail_graph is not None:
+            tail_graph.replay()
+
+
+def _timed_graph(case, steps, warmup, stream, world, sampler):
+    """Time exactly `steps` steps, replayed from CUDA graphs of `chunk`
+    steps (a multiple of the weight-copy count, so the rotation runs on
+    across replays) plus one graph for the remainder."""
+    import torch
+    for i in range(max(warmup, 1)):          # eager warm-up: descriptors, attributes
+        case.step(i, stream)
+    torch.cuda.synchronize()
+    chunk = case.copies * max(1, 32 // case.copies)
+    chunk = min(chunk, max(case.copies, steps))
+    g = _capture(case, chunk, stream)
+    tail = _capture(case, steps % chunk, stream) if steps % chunk else None
+    _replay_steps(stream, max(warmup, chunk), g, chunk, None)   # graph warm-up
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    wall0 = time.time()
+    t0.record(stream)
+    _replay_steps(stream, steps, g, chunk, tail)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    wall1 = time.time()
+    if sampler:
+        sampler.mark(wall0, wall1)
+    return t0.elapsed_time(t1)
+
+
+def time_case(case, steps, warmup, stream, world, sampler=None, graph=True):
+    """(total ms of `steps` steps, [mean ms per launch of each linear]).
+
+    graph=True: steps are replayed from CUDA graphs (the way a decode loop
+    runs); the per-linear launch time comes from timing, the same way, a
+    step restricted to that linear (for one-linear workloads it is the step
+    time).  graph=False: eager launches with CUDA events around each."""
+    import torch
+    n_l = case.launches_per_step
+    if graph:
+        total_ms = _timed_graph(case, steps, warmup, stream, world, sampler)
+        if n_l == 1:
+            return total_ms, [total_ms / steps]
+        launch_ms = []
+        for j in range(n_l):
+            case.only = j
+            try:
+                launch_ms.append(_timed_graph(case, steps, warmup, stream, world, None) / steps)
+            finally:
+                case.only = None
+        return total_ms, launch_ms
     for i in range(warmup):
         case.step(i, stream)
     torch.cuda.synchronize()
-    n_l = case.launches_per_step
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(steps * n_l)] if per_launch else None
+          for _ in range(steps * n_l)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     barrier(world)
@@ -244,29 +315,22 @@ def time_case(case, steps, warmup, stream, world, sampler=None, per_launch=True)
     wall0 = time.time()
     t_start.record(stream)
     for i in range(steps):
-        if per_launch:
-            for j, t in enumerate(case.linears):
-                a, b = ev[i * n_l + j]
-                a.record(stream)
-                case.lib.linear_ex(case.x[j], case.wp[i % case.copies][j],
-                                   case.ws[i % case.copies][j], float(t.global_scale),
-                                   case.flags, out=case.y[j], stream=stream)
-                b.record(stream)
-        else:
-            case.step(i, stream)
+        c = i % case.copies
+        for j, t in enumerate(case.linears):
+            a, b = ev[i * n_l + j]
+            a.record(stream)
+            case.lib.linear_ex(case.x[j], case.wp[c][j], case.ws[c][j], float(t.global_scale),
+                               case.flags, out=case.y[j], stream=stream)
+            b.record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
     barrier(world)
     wall1 = time.time()
     if sampler:
         sampler.mark(wall0, wall1)
-    total_ms = t_start.elapsed_time(t_end)
-    launch_ms = None
-    if per_launch:
-        # per linear: mean launch duration
-        launch_ms = [float(np.mean([ev[i * n_l + j][0].elapsed_time(ev[i * n_l + j][1])
-                                    for i in range(steps)])) for j in range(n_l)]
-    return total_ms, launch_ms
+    launch_ms = [float(np.mean([ev[i * n_l + j][0].elapsed_time(ev[i * n_l + j][1])
+                                for i in range(steps)])) for j in range(n_l)]
+    return t_start.elapsed_time(t_end), launch_ms
 
 
 def e2e_case(case, steps, stream, dev):
@@ -322,8 +386,9 @@ def run_ours(args):
     sampler.start()
     stream = torch.cuda.Stream(dev)
 
-    head = Case(args.workload, lib, dev)
-    total_ms, launch_ms = time_case(head, args.steps, args.warmup, stream, world, sampler)
+    head = Case(args.workload, lib, dev, max_rows=args.max_rows)
+    total_ms, launch_ms = time_case(head, args.steps, args.warmup, stream, world, sampler,
+                                    graph=not args.eager)
     step_s = total_ms / 1e3 / args.steps
     max_step_s = aggregate_max(step_s, world)
     tensor_bound = head.linears[0].M > 32
@@ -359,7 +424,12 @@ def run_ours(args):
             "config": {"workload": head.name, "shapes": [[t.M, t.N, t.K] for t in head.linears],
                        "swiglu": head.w.swiglu, "l2": head.l2_note(),
                        "parallelism": "replicas" if world > 1 else "single GPU"},
-            "roofline": roofline, "gpu_launches": args.steps * head.launches_per_step}
+            "roofline": roofline, "gpu_launches": args.steps * head.launches_per_step,
+            "timing": ("CUDA graphs of consecutive steps, CUDA events on the launching "
+                       "stream around the replays" if not args.eager else
+                       "eager launches, CUDA events around each launch")}
+    if args.max_rows is not None:
+        line["config"]["max_rows"] = args.max_rows
 
     if not args.no_extras:
         e2e_ms, h2d, d2h = e2e_case(head, max(3, min(20, args.steps)), stream, dev)
@@ -373,7 +443,7 @@ def run_ours(args):
             if name == head.name:
                 continue
             c = Case(name, lib, dev)
-            tot, lms = time_case(c, steps, 5, stream, world, sampler)
+            tot, lms = time_case(c, steps, 5, stream, world, sampler, graph=not args.eager)
             ms = tot / steps
             ent = {"ms_per_step": round(ms, 5), "kernel": c.kernel,
                    "launch_us": [round(v * 1e3, 2) for v in lms]}
@@ -386,6 +456,12 @@ def run_ours(args):
             extras[name] = ent
             del c
             torch.cuda.empty_cache()
+        if not args.eager:
+            # the same headline steps launched eagerly, for comparison (host
+            # launch overhead included)
+            e_tot, _ = time_case(head, min(args.steps, 500), 5, stream, world, None,
+                                 graph=False)
+            line["eager_ms_per_step"] = round(e_tot / min(args.steps, 500), 6)
         line["workloads"] = extras
         line["gpu_launches_extras"] = "not in the headline timed region"
     sampler.stop()
@@ -494,6 +570,10 @@ def main(argv=None):
     ap.add_argument("--no-extras", action="store_true",
                     help="headline only: no e2e, other workloads or CPU baseline")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--eager", action="store_true",
+                    help="time eager launches instead of CUDA-graph replays")
+    ap.add_argument("--max-rows", type=int, default=None,
+                    help="cap the activation rows of each linear (small profiling cases)")
     args = ap.parse_args(argv)
     if args.impl == "reference":
         run_reference(args)

@@ -27,11 +27,18 @@
  * Ownership: every buffer belongs to the caller.  The library allocates no
  * device or host memory per call and keeps no state besides per-device
  * attributes it caches on first use (device properties, kernel attributes,
- * the address of its device error word).
+ * the address of its device error word) and a small cache of encoded TMA
+ * descriptors, keyed by every input of the encoding (pointer, sizes, box).
  *
  * Behaviour: calls are asynchronous on `stream`; they validate on the host,
  * launch one kernel, and return without synchronising.  A rejected call
- * launches nothing.  A device-side failure (a pipeline wait that timed out)
+ * launches nothing.  Kernels are launched with programmatic dependent
+ * launch: the prologue and the weight/scale prefetch of a call may overlap
+ * the tail of the kernel before it in the stream, while the activations are
+ * read, and the output written, only after that kernel has completed.  So
+ * the weights and scales must not be written by the kernel immediately
+ * before the call in the same stream.  Calls may be captured into a CUDA
+ * graph; a captured call keeps the pointers it was given.  A device-side failure (a pipeline wait that timed out)
  * does not fault the context: the kernel winds down and sets a bit in the
  * library's device error word, readable with nvfp4_device_status().
  *
@@ -61,6 +68,25 @@ extern "C" {
 #define NVFP4_FLAG_F32_OUT 2u       /* write fp32 (before bf16 rounding) */
 #define NVFP4_FLAG_FORCE_SMALLM 4u  /* force the few-row kernel (needs M <= 32) */
 #define NVFP4_FLAG_FORCE_TCGEMM 8u  /* force the tcgen05 tensor-core kernel */
+/* Tuning override of the few-row kernel: split k over n CTAs of one
+ * thread-block cluster (1 <= n <= 16) instead of the built-in choice;
+ * n = 0 means automatic.  Encode with NVFP4_FLAG_SPLIT(n). */
+#define NVFP4_FLAG_SPLIT_SHIFT 8
+#define NVFP4_FLAG_SPLIT_MASK (0x1Fu << NVFP4_FLAG_SPLIT_SHIFT)
+#define NVFP4_FLAG_SPLIT(n) (((unsigned int)(n) & 0x1Fu) << NVFP4_FLAG_SPLIT_SHIFT)
+/* Tuning override of the few-row kernel: CTAs of 16 * n weight rows
+ * (1 <= n <= 8, at most 4 when M > 16) instead of the built-in choice;
+ * n = 0 means automatic.  A combination that does not fit on the device is
+ * rejected with NVFP4_ERR_INVALID. */
+#define NVFP4_FLAG_GROUPS_SHIFT 13
+#define NVFP4_FLAG_GROUPS_MASK (0xFu << NVFP4_FLAG_GROUPS_SHIFT)
+#define NVFP4_FLAG_GROUPS(n) (((unsigned int)(n) & 0xFu) << NVFP4_FLAG_GROUPS_SHIFT)
+/* Few-row kernel with M <= 8: multiply in bf16, the activations as given,
+ * instead of the default f16 path.  The f16 path converts each activation
+ * row to f16 after scaling it by a power of two taken from the row's
+ * running maximum |x|; it is exact for every activation within a factor
+ * 2^31 of that maximum and otherwise rounds it like an f16 subnormal. */
+#define NVFP4_FLAG_BF16_MMA (1u << 17)
 
 /* Kernel identifiers returned by nvfp4_linear_kernel_for. */
 #define NVFP4_KERNEL_NONE 0

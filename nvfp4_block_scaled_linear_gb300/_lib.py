@@ -19,6 +19,19 @@ FLAG_SWIGLU = 1
 FLAG_F32_OUT = 2
 FLAG_FORCE_SMALLM = 4
 FLAG_FORCE_TCGEMM = 8
+FLAG_BF16_MMA = 1 << 17
+
+
+def FLAG_SPLIT(n):
+    """Few-row kernel: split k over n CTAs of one cluster (1..16)."""
+    return (int(n) & 0x1F) << 8
+
+
+def FLAG_GROUPS(n):
+    """Few-row kernel: CTAs of 16*n weight rows (1..8)."""
+    return (int(n) & 0xF) << 13
+
+
 KERNEL_NONE, KERNEL_SMALLM, KERNEL_TCGEMM = 0, 1, 2
 KERNEL_NAMES = {KERNEL_SMALLM: "smallm", KERNEL_TCGEMM: "tcgemm"}
 

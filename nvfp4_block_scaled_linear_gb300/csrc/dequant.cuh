@@ -5,25 +5,38 @@
 // byte (low nibble = even k), weight_scale holds one fp8 e4m3 per 16 inputs.
 //
 // A code times a block scale has at most 2 x 4 significant bits, so the
-// product is exact in bf16.  The kernels therefore feed exact bf16 weights
-// to the tensor cores and apply the fp32 global scale once, in the epilogue.
+// product is exact in bf16 and in f16.  The kernels therefore feed exact
+// weights to the tensor cores and apply the fp32 global scale once, in the
+// epilogue.
 //
-// Bit trick.  Placing a code's three magnitude bits (e1 e0 m) at bf16 bits
-// 8..6 and its sign at bit 15 gives the bf16 number code * 2^-126: the two
-// exponent bits land in the low end of the bf16 exponent field, the mantissa
-// bit at the top of the mantissa, and exponent 0 (the e2m1 subnormals 0 and
-// 0.5) lands on bf16's own subnormals.  One bf16 multiply by
+// bf16 bit trick.  Placing a code's three magnitude bits (e1 e0 m) at bf16
+// bits 8..6 and its sign at bit 15 gives the bf16 number code * 2^-126: the
+// two exponent bits land in the low end of the bf16 exponent field, the
+// mantissa bit at the top of the mantissa, and exponent 0 (the e2m1
+// subnormals 0 and 0.5) lands on bf16's own subnormals.  One bf16 multiply by
 // S = scale * 2^116 then yields code * scale * 2^-10 exactly (2^-20 at the
 // smallest, so never subnormal); the epilogue multiplies by 2^10.
+//
+// f16 path.  The hardware converts two e2m1 codes to f16x2 in one
+// instruction; one f16x2 multiply by the scale gives code * scale exactly
+// (between 2^-10 and 2688 in magnitude: normal f16 numbers).
 #pragma once
 #include <cstdint>
+#include <cuda_fp16.h>
 
 #include "ptx.cuh"
 
 namespace nvfp4 {
 
-// Exponent offset folded into the dequantised weights; undone in the epilogue.
+// Exponent offset folded into the bf16 dequantised weights; undone in the
+// epilogue, which multiplies the fp32 accumulator by fp32(2^10 / global_scale).
 constexpr float kWeightPow2 = 1024.0f;   // 2^10
+
+// SwiGLU epilogue: silu(g) * u = g / (1 + e^-g) * u, in fp32 with the CUDA
+// fast exponential and a correctly rounded reciprocal (e^-g = inf gives 0).
+__device__ __forceinline__ float silu_mul(float g, float u) {
+  return g * __frcp_rn(1.0f + __expf(-g)) * u;
+}
 
 // bf16x2 (S, S) for an e4m3 bit pattern, S = value * 2^116; NaN for S.1111.111.
 // Exact: an e4m3 value has at most 4 significant bits.
@@ -44,17 +57,46 @@ __device__ __forceinline__ uint32_t scale_pair_from_e4m3(uint32_t b) {
   return h | (h << 16);
 }
 
-// Eight codes (one 32-bit word, k = 0..7 in nibble order) times the pair
-// scale S -> four bf16x2 words pairing (k, k+4):
+// f16x2 (S, S) for an e4m3 bit pattern, S = its value (exact in f16); NaN
+// for S.1111.111.
+__device__ __forceinline__ uint32_t scale_pair_f16_from_e4m3(uint32_t b) {
+  const uint32_t e = (b >> 3) & 15u, m = b & 7u;
+  uint32_t h;
+  if (e == 15u && m == 7u)
+    h = 0x7E00u;                                   // NaN
+  else if (e != 0u)
+    h = ((e + 8u) << 10) | (m << 7);               // 2^(e-7) (1 + m/8), f16 bias 15
+  else
+    h = __half_as_ushort(__float2half_rn(static_cast<float>(m) * 0x1p-9f));  // m 2^-9
+  h |= (b & 0x80u) << 8;                           // sign
+  return h | (h << 16);
+}
+
+// Integer shifts by a constant, written as multiplies so that they issue on
+// the FMA pipe (IMAD) rather than the integer/logic pipe, which the masks
+// below already keep busy.
+__device__ __forceinline__ uint32_t shl_fma(uint32_t w, uint32_t pow2) {
+  uint32_t d;
+  asm("mul.lo.u32 %0, %1, %2;" : "=r"(d) : "r"(w), "r"(pow2));
+  return d;
+}
+__device__ __forceinline__ uint32_t shr_fma(uint32_t w, uint32_t pow2_32_minus_s) {
+  uint32_t d;
+  asm("mul.hi.u32 %0, %1, %2;" : "=r"(d) : "r"(w), "r"(pow2_32_minus_s));
+  return d;
+}
+
+// Eight codes (one 32-bit word, k = 0..7 in nibble order) times the bf16
+// pair scale S -> four bf16x2 words pairing (k, k+4):
 //   out[i] = ( w(k=i), w(k=i+4) ),  i = 0..3,
-// each w = code * scale * 2^-10.  Callers that need consecutive k use
-// pair_consecutive() below.
+// each w = code * scale * 2^-10.  Pair i needs its magnitude bits moved by
+// 6 - 4i and its sign bits by 12 - 4i.
 __device__ __forceinline__ void dequant8_strided(uint32_t w, uint32_t S, uint32_t* out) {
   const uint32_t kMag = 0x01C001C0u, kSign = 0x80008000u;
-  const uint32_t r0 = ((w << 6) & kMag) | ((w << 12) & kSign);
-  const uint32_t r1 = ((w << 2) & kMag) | ((w << 8) & kSign);
-  const uint32_t r2 = ((w >> 2) & kMag) | ((w << 4) & kSign);
-  const uint32_t r3 = ((w >> 6) & kMag) | (w & kSign);
+  const uint32_t r0 = (shl_fma(w, 1u << 6) & kMag) | (shl_fma(w, 1u << 12) & kSign);
+  const uint32_t r1 = (shl_fma(w, 1u << 2) & kMag) | (shl_fma(w, 1u << 8) & kSign);
+  const uint32_t r2 = (shr_fma(w, 1u << 30) & kMag) | (shl_fma(w, 1u << 4) & kSign);
+  const uint32_t r3 = (shr_fma(w, 1u << 26) & kMag) | (w & kSign);
   out[0] = bf16x2_mul(r0, S);
   out[1] = bf16x2_mul(r1, S);
   out[2] = bf16x2_mul(r2, S);
@@ -68,6 +110,16 @@ __device__ __forceinline__ void pair_consecutive(const uint32_t* p, uint32_t* ou
   out[1] = prmt(p[2], p[3], 0x5410u);   // k2 | k3
   out[2] = prmt(p[0], p[1], 0x7632u);   // k4 | k5
   out[3] = prmt(p[2], p[3], 0x7632u);   // k6 | k7
+}
+
+// Eight codes (one 32-bit word, k = 0..7 in order) times the f16 pair scale
+// S -> four f16x2 words of consecutive k: out[j] = (w(2j), w(2j+1)), each
+// w = code * scale exactly.
+__device__ __forceinline__ void dequant8_f16(uint32_t w, uint32_t S, uint32_t* out) {
+  out[0] = f16x2_mul(cvt_e2m1x2_f16x2(w), S);
+  out[1] = f16x2_mul(cvt_e2m1x2_f16x2(w >> 8), S);
+  out[2] = f16x2_mul(cvt_e2m1x2_f16x2(w >> 16), S);
+  out[3] = f16x2_mul(cvt_e2m1x2_f16x2(w >> 24), S);
 }
 
 }  // namespace nvfp4

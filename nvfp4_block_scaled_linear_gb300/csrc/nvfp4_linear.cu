@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -14,7 +15,12 @@
 
 namespace {
 
-using nvfp4::smallm::Layout;
+namespace sm = nvfp4::smallm;
+
+// Weight and scale bytes one 16-row group brings per 256-k stage, and the
+// weight bytes an SM should keep in flight (HBM latency x its bandwidth share).
+constexpr double kGroupBytesPerStage = 16.0 * (256 / 2 + 256 / 16);
+constexpr double kWantInFlight = 128.0 * 1024;
 
 // Bits set by kernels when a pipeline wait gives up (see ptx.cuh).
 __device__ unsigned int g_device_error;
@@ -22,29 +28,72 @@ __device__ unsigned int g_device_error;
 constexpr int kMaxDevices = 64;
 constexpr int64_t kSmallMMax = 32;
 
+using SmallmFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, sm::Params);
+
+// The few-row kernel instance for (MT, G, f16); combinations the kernel does
+// not support are never instantiated.
+template <int MT, int G, bool F16>
+constexpr SmallmFn smallm_instance() {
+  if constexpr (G <= sm::max_groups(MT) && (!F16 || MT == 1))
+    return &sm::smallm_kernel<MT, G, F16>;
+  else
+    return nullptr;
+}
+template <int MT, bool F16>
+SmallmFn smallm_fn(int g) {
+  switch (g) {
+    case 1: return smallm_instance<MT, 1, F16>();
+    case 2: return smallm_instance<MT, 2, F16>();
+    case 3: return smallm_instance<MT, 3, F16>();
+    case 4: return smallm_instance<MT, 4, F16>();
+    case 5: return smallm_instance<MT, 5, F16>();
+    case 6: return smallm_instance<MT, 6, F16>();
+    case 7: return smallm_instance<MT, 7, F16>();
+    case 8: return smallm_instance<MT, 8, F16>();
+    default: return nullptr;
+  }
+}
+
 struct DeviceInfo {
   bool ready = false;
   bool supported = false;
   int num_sms = 0;
+  int max_smem = 0;                    // opt-in shared memory per block
+  int smem_per_sm = 0, smem_reserved = 0, regs_per_sm = 0, threads_per_sm = 0;
   unsigned int* err = nullptr;         // device address of g_device_error
-  int smallm_ctas_per_sm[5] = {0, 0, 0, 0, 0};   // by MT
+  int smallm_regs[2][5][sm::kMaxGroups + 1] = {};  // registers per thread by (f16, MT, G)
 };
 
 std::mutex g_mutex;
 DeviceInfo g_dev[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
-template <int MT>
+template <int MT, bool F16>
 cudaError_t prepare_smallm(DeviceInfo& d) {
-  auto kern = nvfp4::smallm::smallm_kernel<MT>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       Layout<MT>::kSmemBytes);
-  if (e != cudaSuccess) return e;
-  int n = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, nvfp4::smallm::kThreads,
-                                                    Layout<MT>::kSmemBytes);
-  d.smallm_ctas_per_sm[MT] = n > 0 ? n : 1;
-  return e;
+  for (int g = 1; g <= sm::max_groups(MT); ++g) {
+    const SmallmFn kern = smallm_fn<MT, F16>(g);
+    if (!kern) continue;
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, d.max_smem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    cudaFuncAttributes fa;
+    if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    d.smallm_regs[F16 ? 1 : 0][MT][g] = fa.numRegs;
+  }
+  return cudaSuccess;
+}
+
+// Resident CTAs per SM for a block of `threads` threads using `regs`
+// registers each and `smem` bytes of dynamic shared memory.
+int resident_ctas(const DeviceInfo& d, int threads, int regs, int smem) {
+  const int warps = (threads + 31) / 32;
+  const int regs_per_warp = (regs * 32 + 255) / 256 * 256;
+  int n = d.smem_per_sm / (smem + d.smem_reserved);
+  if (regs_per_warp > 0) n = std::min(n, d.regs_per_sm / (regs_per_warp * warps));
+  n = std::min(n, d.threads_per_sm / threads);
+  return std::max(0, std::min(n, 32));
 }
 
 // Per-device, one-time set-up.  Returns a status.
@@ -64,6 +113,11 @@ int device_setup(DeviceInfo** out) {
     }
     d.supported = (prop.major == 10 && prop.minor == 3);
     d.num_sms = prop.multiProcessorCount;
+    d.max_smem = static_cast<int>(prop.sharedMemPerBlockOptin);
+    d.smem_per_sm = static_cast<int>(prop.sharedMemPerMultiprocessor);
+    d.smem_reserved = static_cast<int>(prop.reservedSharedMemPerBlock);
+    d.regs_per_sm = prop.regsPerMultiprocessor;
+    d.threads_per_sm = prop.maxThreadsPerMultiProcessor;
     if (d.supported) {
       if (!g_encode) {
         void* fn = nullptr;
@@ -78,8 +132,11 @@ int device_setup(DeviceInfo** out) {
       }
       void* err_addr = nullptr;
       if (cudaGetSymbolAddress(&err_addr, g_device_error) != cudaSuccess ||
-          prepare_smallm<1>(d) != cudaSuccess || prepare_smallm<2>(d) != cudaSuccess ||
-          prepare_smallm<3>(d) != cudaSuccess || prepare_smallm<4>(d) != cudaSuccess ||
+          prepare_smallm<1, false>(d) != cudaSuccess ||
+          prepare_smallm<2, false>(d) != cudaSuccess ||
+          prepare_smallm<3, false>(d) != cudaSuccess ||
+          prepare_smallm<4, false>(d) != cudaSuccess ||
+          prepare_smallm<1, true>(d) != cudaSuccess ||
           cudaFuncSetAttribute(nvfp4::tcgemm::tcgemm_kernel,
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                nvfp4::tcgemm::kSmemBytes) != cudaSuccess) {
@@ -95,16 +152,65 @@ int device_setup(DeviceInfo** out) {
   return NVFP4_OK;
 }
 
+// Encoding a tensor map costs microseconds of host time, comparable to a
+// decode-sized kernel, so encoded maps are kept in a small direct-mapped
+// cache.  The key holds every encoding input, so a hit is always valid.
+struct MapKey {
+  const void* base;
+  uint64_t dim0, dim1, row_bytes;
+  uint32_t box0, box1;
+  int dtype, swizzle;
+  bool operator==(const MapKey& o) const {
+    return base == o.base && dim0 == o.dim0 && dim1 == o.dim1 && row_bytes == o.row_bytes &&
+           box0 == o.box0 && box1 == o.box1 && dtype == o.dtype && swizzle == o.swizzle;
+  }
+};
+struct MapSlot {
+  bool valid = false;
+  MapKey key{};
+  CUtensorMap map{};
+};
+constexpr int kMapCacheSlots = 256;
+MapSlot g_map_cache[kMapCacheSlots];
+std::mutex g_map_mutex;
+
 bool encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t dim0,
                uint64_t dim1, uint64_t row_bytes, uint32_t box0, uint32_t box1,
                CUtensorMapSwizzle swizzle) {
+  const MapKey key{base, dim0, dim1, row_bytes, box0, box1, static_cast<int>(dtype),
+                   static_cast<int>(swizzle)};
+  uint64_t h = reinterpret_cast<uintptr_t>(base) >> 4;
+  h ^= dim0 * 0x9E3779B97F4A7C15ull ^ dim1 * 0xC2B2AE3D27D4EB4Full ^ (uint64_t(box1) << 20) ^
+       (uint64_t(box0) << 7) ^ uint64_t(swizzle) ^ (uint64_t(dtype) << 3);
+  h ^= h >> 29;
+  MapSlot& slot = g_map_cache[h % kMapCacheSlots];
+  {
+    std::lock_guard<std::mutex> lock(g_map_mutex);
+    if (slot.valid && slot.key == key) {
+      *map = slot.map;
+      return true;
+    }
+  }
   const cuuint64_t dims[2] = {dim0, dim1};
   const cuuint64_t strides[1] = {row_bytes};
   const cuuint32_t box[2] = {box0, box1};
   const cuuint32_t estr[2] = {1, 1};
-  return g_encode(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  if (g_encode(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  std::lock_guard<std::mutex> lock(g_map_mutex);
+  slot.valid = true;
+  slot.key = key;
+  slot.map = *map;
+  return true;
+}
+
+// The global scale is applied as one fp32 multiply by 2^10 / global_scale
+// (2^10 undoes the exponent offset of the bf16 dequantised weights).
+float out_scale(float global_scale) {
+  return static_cast<float>(static_cast<double>(nvfp4::kWeightPow2) /
+                            static_cast<double>(global_scale));
 }
 
 int validate(const void* x, const void* wp, const void* ws, const void* y, int64_t M,
@@ -114,7 +220,11 @@ int validate(const void* x, const void* wp, const void* ws, const void* y, int64
   // null data pointer is fine there.
   if (!wp || !ws || (M > 0 && (!x || !y))) return NVFP4_ERR_INVALID;
   if (flags & ~(NVFP4_FLAG_SWIGLU | NVFP4_FLAG_F32_OUT | NVFP4_FLAG_FORCE_SMALLM |
-                NVFP4_FLAG_FORCE_TCGEMM))
+                NVFP4_FLAG_FORCE_TCGEMM | NVFP4_FLAG_SPLIT_MASK | NVFP4_FLAG_GROUPS_MASK |
+                NVFP4_FLAG_BF16_MMA))
+    return NVFP4_ERR_INVALID;
+  if (((flags & NVFP4_FLAG_SPLIT_MASK) >> NVFP4_FLAG_SPLIT_SHIFT) > sm::kMaxSplit ||
+      ((flags & NVFP4_FLAG_GROUPS_MASK) >> NVFP4_FLAG_GROUPS_SHIFT) > sm::kMaxGroups)
     return NVFP4_ERR_INVALID;
   if ((flags & NVFP4_FLAG_FORCE_SMALLM) && (flags & NVFP4_FLAG_FORCE_TCGEMM))
     return NVFP4_ERR_INVALID;
@@ -135,56 +245,128 @@ int kernel_for(int64_t M, unsigned int flags) {
   return M <= kSmallMMax ? NVFP4_KERNEL_SMALLM : NVFP4_KERNEL_TCGEMM;
 }
 
-template <int MT>
+struct SmallmPlan {
+  int groups = 0;
+  int split = 0;
+  int stages = 0;
+  int64_t row_blocks = 0;
+};
+
+// Choose the CTA height (G groups of 16 rows), the k split and the ring
+// depth.  Cost model: the work of the busiest SM, ceil(CTAs / SMs) x
+// (G x stages per CTA + a fixed per-CTA cost of two stages), inflated when
+// the rings of an SM hold less than ~128 KB of weights in flight; grids that
+// are resident in one wave win over those that are not; ties go to fewer
+// CTAs.  Overrides in `flags` pin G or the split.
+template <int MT, bool F16>
+SmallmPlan plan_smallm(const DeviceInfo& d, int64_t M, int64_t N, int64_t K,
+                       unsigned int flags) {
+  const bool swiglu = flags & NVFP4_FLAG_SWIGLU;
+  const int64_t T = K / sm::kStageK;
+  const int want_split = (flags & NVFP4_FLAG_SPLIT_MASK) >> NVFP4_FLAG_SPLIT_SHIFT;
+  const int want_groups = (flags & NVFP4_FLAG_GROUPS_MASK) >> NVFP4_FLAG_GROUPS_SHIFT;
+  const int64_t unit_rows = swiglu ? N / 2 : N;
+  const int threads = sm::threads_for(F16);
+  static const int kStageChoices[] = {3, 4, 5, 6, 8};
+  SmallmPlan best;
+  double best_cost = -1.0;
+  int64_t best_ctas = 0;
+  bool best_one_wave = false;
+  for (int g = 1; g <= sm::max_groups(MT); ++g) {
+    if (want_groups && g != want_groups) continue;
+    const int regs = d.smallm_regs[F16 ? 1 : 0][MT][g];
+    if (regs <= 0) continue;
+    const int64_t rows_per_cta = swiglu ? 8 * g : 16 * g;
+    const int64_t row_blocks = (unit_rows + rows_per_cta - 1) / rows_per_cta;
+    for (int stages : kStageChoices) {
+      const sm::SmemLayout lay = sm::make_layout(MT, g, stages, F16, static_cast<int>(M));
+      if (lay.total > d.max_smem || !sm::layout_ok(lay, MT, g)) continue;
+      const int occ = resident_ctas(d, threads, regs, lay.total);
+      if (occ <= 0) continue;
+      const int64_t slots = static_cast<int64_t>(d.num_sms) * occ;
+      const int s_max = want_split ? want_split : 8;
+      for (int s = 1; s <= s_max && s <= T; ++s) {
+        if (want_split && s != want_split) continue;
+        const int64_t ctas = row_blocks * s;
+        const bool one_wave = ctas <= slots;
+        const int64_t per_sm = (ctas + d.num_sms - 1) / d.num_sms;
+        const double in_flight = static_cast<double>(std::min<int64_t>(per_sm, occ)) *
+                                 (stages - 1) * g * kGroupBytesPerStage;
+        double cost = static_cast<double>(per_sm) * g * ((T + s - 1) / s + 2);
+        if (in_flight < kWantInFlight) cost *= kWantInFlight / in_flight;
+        const bool better =
+            best_cost < 0 || (one_wave && !best_one_wave) ||
+            (one_wave == best_one_wave &&
+             (cost < best_cost * 0.999 || (cost <= best_cost * 1.001 && ctas < best_ctas)));
+        if (better) {
+          best_cost = cost;
+          best_ctas = ctas;
+          best_one_wave = one_wave;
+          best.groups = g;
+          best.split = s;
+          best.stages = stages;
+          best.row_blocks = row_blocks;
+        }
+      }
+    }
+  }
+  return best;
+}
+
+template <int MT, bool F16>
 int launch_smallm(const DeviceInfo& d, const void* x, const uint8_t* wp, const uint8_t* ws,
                   float gs, void* y, int64_t M, int64_t N, int64_t K, unsigned int flags,
                   cudaStream_t stream) {
-  using L = Layout<MT>;
   const bool swiglu = flags & NVFP4_FLAG_SWIGLU;
+  const SmallmPlan plan = plan_smallm<MT, F16>(d, M, N, K, flags);
+  if (plan.groups == 0) return NVFP4_ERR_INVALID;   // overrides that cannot run
+  const int half_rows = 8 * plan.groups;
   CUtensorMap tw, ts, tx;
-  if (!encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, wp, K / 2, N, K / 2, 128,
-                 nvfp4::smallm::kHalfRows, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !encode_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT8, ws, K / 16, N, K / 16, 16,
-                 nvfp4::smallm::kHalfRows, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-      !encode_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, K, M, K * 2, 64, MT * 8,
-                 CU_TENSOR_MAP_SWIZZLE_128B))
+  const bool x_ok =
+      MT == 1 ? encode_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, K, M, K * 2, sm::kStageK,
+                          static_cast<uint32_t>(M), CU_TENSOR_MAP_SWIZZLE_NONE)
+              : encode_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, K, M, K * 2, 64, MT * 8,
+                          CU_TENSOR_MAP_SWIZZLE_128B);
+  if (!encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, wp, K / 2, N, K / 2, 128, half_rows,
+                 CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT8, ws, K / 16, N, K / 16, 16, half_rows,
+                 CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !x_ok)
     return NVFP4_ERR_LAUNCH;
 
-  nvfp4::smallm::Params p;
+  sm::Params p;
   p.y = y;
   p.M = M;
   p.N = N;
   p.K = K;
-  p.global_scale = gs;
-  p.stages_total = static_cast<int>(K / nvfp4::smallm::kStageK);
+  // f16 weights are exact code * scale; the bf16 ones carry 2^-10
+  p.out_scale = F16 ? static_cast<float>(1.0 / static_cast<double>(gs)) : out_scale(gs);
+  p.stages_total = static_cast<int>(K / sm::kStageK);
+  p.split = plan.split;
+  p.lay = sm::make_layout(MT, plan.groups, plan.stages, F16, static_cast<int>(M));
   p.out_f32 = (flags & NVFP4_FLAG_F32_OUT) ? 1 : 0;
   p.swiglu = swiglu ? 1 : 0;
   p.err = d.err;
 
-  const int64_t row_blocks =
-      swiglu ? (N / 2) / nvfp4::smallm::kHalfRows : N / nvfp4::smallm::kRows;
-  // Split k across a cluster when the row blocks alone cannot fill the GPU.
-  const int64_t slots = static_cast<int64_t>(d.num_sms) * d.smallm_ctas_per_sm[MT];
-  int64_t split = row_blocks >= slots ? 1 : slots / row_blocks;
-  if (split > 8) split = 8;
-  if (split > p.stages_total) split = p.stages_total;
-  if (split < 1) split = 1;
-  p.split = static_cast<int>(split);
-
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof cfg);
-  cfg.gridDim = dim3(static_cast<unsigned>(row_blocks), static_cast<unsigned>(split), 1);
-  cfg.blockDim = dim3(nvfp4::smallm::kThreads, 1, 1);
-  cfg.dynamicSmemBytes = L::kSmemBytes;
+  cfg.gridDim = dim3(static_cast<unsigned>(plan.row_blocks), static_cast<unsigned>(plan.split), 1);
+  cfg.blockDim = dim3(sm::threads_for(F16), 1, 1);
+  cfg.dynamicSmemBytes = p.lay.total;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 1;
-  attr[0].val.clusterDim.y = static_cast<unsigned>(split);
+  attr[0].val.clusterDim.y = static_cast<unsigned>(plan.split);
   attr[0].val.clusterDim.z = 1;
+  // Programmatic dependent launch: the prologue and the weight prefetch may
+  // overlap the tail of the preceding kernel in the stream.
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, nvfp4::smallm::smallm_kernel<MT>, tw, ts, tx, p);
+  cfg.numAttrs = 2;
+  const cudaError_t e =
+      cudaLaunchKernelEx(&cfg, smallm_fn<MT, F16>(plan.groups), tw, ts, tx, p);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return NVFP4_ERR_LAUNCH;
@@ -210,16 +392,28 @@ int launch_tcgemm(const DeviceInfo& d, const void* x, const uint8_t* wp, const u
   p.M = M;
   p.N = N;
   p.K = K;
-  p.global_scale = gs;
+  p.out_scale = out_scale(gs);
   p.out_f32 = (flags & NVFP4_FLAG_F32_OUT) ? 1 : 0;
   p.swiglu = swiglu ? 1 : 0;
   p.err = d.err;
-  const unsigned gx = static_cast<unsigned>(swiglu ? (N / 2) / 64 : N / T::kTileW);
-  const unsigned gy = static_cast<unsigned>((M + T::kTileX - 1) / T::kTileX);
-  T::tcgemm_kernel<<<dim3(gx, gy, 1), T::kThreads, T::kSmemBytes, stream>>>(tx, tw, ts, p);
-  const cudaError_t e = cudaGetLastError();
-  return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_LAUNCH;
-  (void)d;
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof cfg);
+  cfg.gridDim = dim3(static_cast<unsigned>(swiglu ? (N / 2) / 64 : N / T::kTileW),
+                     static_cast<unsigned>((M + T::kTileX - 1) / T::kTileX), 1);
+  cfg.blockDim = dim3(T::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = T::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, T::tcgemm_kernel, tx, tw, ts, p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return NVFP4_ERR_LAUNCH;
+  }
+  return NVFP4_OK;
 }
 
 int run(const void* x, const uint8_t* wp, const uint8_t* ws, float gs, void* y, int64_t M,
@@ -233,10 +427,13 @@ int run(const void* x, const uint8_t* wp, const uint8_t* ws, float gs, void* y, 
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   if (kernel_for(M, flags) == NVFP4_KERNEL_SMALLM) {
     switch ((M + 7) / 8) {
-      case 1: return launch_smallm<1>(*d, x, wp, ws, gs, y, M, N, K, flags, stream);
-      case 2: return launch_smallm<2>(*d, x, wp, ws, gs, y, M, N, K, flags, stream);
-      case 3: return launch_smallm<3>(*d, x, wp, ws, gs, y, M, N, K, flags, stream);
-      default: return launch_smallm<4>(*d, x, wp, ws, gs, y, M, N, K, flags, stream);
+      case 1:
+        if (!(flags & NVFP4_FLAG_BF16_MMA))
+          return launch_smallm<1, true>(*d, x, wp, ws, gs, y, M, N, K, flags, stream);
+        return launch_smallm<1, false>(*d, x, wp, ws, gs, y, M, N, K, flags, stream);
+      case 2: return launch_smallm<2, false>(*d, x, wp, ws, gs, y, M, N, K, flags, stream);
+      case 3: return launch_smallm<3, false>(*d, x, wp, ws, gs, y, M, N, K, flags, stream);
+      default: return launch_smallm<4, false>(*d, x, wp, ws, gs, y, M, N, K, flags, stream);
     }
   }
   return launch_tcgemm(*d, x, wp, ws, gs, y, M, N, K, flags, stream);

@@ -4,25 +4,38 @@
 // the packed weights and scales from HBM once; every design choice below is
 // about keeping that stream at full rate.
 //
-//  * One CTA owns 64 weight rows and a contiguous range of k.  A producer
-//    warp streams 256-k stages (packed weights, block scales, activations)
-//    into a shared-memory ring with TMA; an L2 evict-first hint keeps the
-//    once-read weights from displacing the activations.
-//  * Four consumer warps each take a 64-k quarter of every stage for all 64
-//    rows.  The weights are dequantised in registers straight into the A
-//    fragments of the register-fed m16n8k16 bf16 warp MMA (weights as the
-//    16-row operand, activations as the 8-wide one), so the dequantised
-//    weights never touch shared memory.  (The tcgen05 MMA reads both of its
-//    operands from shared memory or TMEM; at N = 8..32 that round trip would
-//    cost more shared-memory bandwidth than the weight stream itself.)
-//  * k is permuted inside each thread's 16-element block so that the cheap
-//    (k, k+4) pairing of the dequantiser is used unchanged; the activation
-//    fragments are built with the same permutation, so the dot products are
-//    unchanged.
+//  * One CTA owns G groups of 16 weight rows (G = 1..8, chosen per call) and
+//    a contiguous range of k.  A producer warp streams 256-k stages (packed
+//    weights, block scales, activations) into a shared-memory ring with TMA;
+//    an L2 evict-first hint keeps the once-read weights from displacing the
+//    activations.  The weights of the first ring-full are requested before
+//    the kernel waits on the preceding kernel in the stream (programmatic
+//    dependent launch); the activations only after.
+//  * Eight consumer warps: warp (kq, rp) takes the 64-k quarter kq of every
+//    stage for the row groups rp, rp+2, rp+4, rp+6 of the CTA.  The weights
+//    are dequantised in registers straight into the A fragments of the
+//    register-fed m16n8k16 warp MMA (weights as the 16-row operand,
+//    activations as the 8-wide one), so dequantised weights never touch
+//    shared memory.  (The tcgen05 MMA reads both of its operands from shared
+//    memory or TMEM; at N = 8..32 that round trip would cost more shared-memory
+//    bandwidth than the weight stream itself.)
+//  * bf16 path (any M <= 32): the dequantiser's (k, k+4) pairing is matched
+//    by building the activation fragments with the same k permutation, so
+//    the dot products are unchanged.
+//  * f16 path (M <= 8, the default there): the weights are dequantised by the
+//    hardware e2m1 -> f16 conversion, about half the instructions of the bf16
+//    bit manipulation, so the MMA runs in f16 and a converter warp brings the
+//    activations to f16 each stage with a power-of-two scale per activation
+//    row, taken from that row's running maximum |x|.  Every activation within
+//    2^31 of its row's running maximum converts exactly, nothing overflows,
+//    and the fp32 accumulators are rescaled by exact powers of two when a
+//    row's maximum grows.
 //  * Split-K: CTAs that share rows but not k form one thread-block cluster.
 //    Partials are reduced warp -> CTA in shared memory and then across the
 //    cluster through distributed shared memory.  No global workspace, no
 //    atomics, no spin-waits on other CTAs.
+//  * The host picks G, the split and the ring depth so that the whole grid is
+//    resident at once and the busiest SM carries as little work as possible.
 #pragma once
 #include <cstdint>
 #include <cuda_bf16.h>
@@ -33,56 +46,119 @@
 namespace nvfp4 {
 namespace smallm {
 
-constexpr int kRows = 64;             // weight rows per CTA
-constexpr int kHalfRows = 32;         // rows per TMA box (two boxes per stage)
+constexpr int kGroupRows = 16;        // rows of one MMA row group
+constexpr int kMaxGroups = 8;         // up to 128 weight rows per CTA
 constexpr int kStageK = 256;          // k per pipeline stage
-constexpr int kConsumerWarps = 4;     // one 64-k quarter of a stage each
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
-constexpr int kWBytes = kRows * kStageK / 2;       // 8 KB packed weights
-constexpr int kSBytes = kRows * kStageK / 16;      // 1 KB block scales
-constexpr int kSOff = kWBytes;
-constexpr int kXOff = kWBytes + kSBytes;           // 9 KB, 1024-aligned
+constexpr int kKQuarters = 4;         // 64-k quarters of a stage
+constexpr int kConsumerWarps = 8;     // (k quarter, row-group parity)
+constexpr int kMaxSplit = 16;         // cluster size limit (non-portable above 8)
+constexpr int kF16MaxRows = 8;        // the f16 path serves M <= 8
 
-template <int MT>
-struct Layout {
-  static constexpr int kXBoxBytes = MT * 8 * 128;            // 64 k x MT*8 rows
-  static constexpr int kStageBytes = kXOff + kConsumerWarps * kXBoxBytes;
-  static constexpr int kStages = (MT <= 2) ? 4 : 4;
-  static constexpr int kRingBytes = kStageBytes * kStages;
-  static constexpr int kRedFloats = kConsumerWarps * kRows * MT * 8;
-  static constexpr int kPartOff = kRingBytes;                // CTA partials
-  static constexpr int kPartBytes = kRows * MT * 8 * 4;
-  static constexpr int kLutOff = kPartOff + kPartBytes;
-  static constexpr int kBarOff = kLutOff + 256 * 4;
-  static constexpr int kSmemBytes = kBarOff + 2 * kStages * 8 + 16 + 1024;  // + align
-  static_assert(kRedFloats * 4 <= kRingBytes, "reduction buffer must fit the ring");
+// Consumers, the TMA producer and (f16 path) the activation converter.
+__host__ __device__ constexpr int threads_for(bool f16) {
+  return (kConsumerWarps + 1 + (f16 ? 1 : 0)) * 32;
+}
+
+// Row groups one consumer warp may hold: all of its accumulators live in
+// registers, so the widest activation tiles get fewer.
+__host__ __device__ constexpr int groups_per_warp(int mt) { return mt <= 2 ? 4 : 2; }
+__host__ __device__ constexpr int max_groups(int mt) { return 2 * groups_per_warp(mt); }
+
+// Shared-memory layout of one launch (byte offsets from the 1024-aligned
+// base), computed on the host per call.  Stage: packed weights
+// [16G rows][128 B] (128B-swizzled), block scales [16G rows][16 B], then the
+// activations: for M <= 8 one plain box [M rows][256 k] bf16 and (f16 path)
+// its f16 copy [M rows][256 k] plus the rows' exponents; for larger M four
+// 128B-swizzled boxes [MT*8 rows][64 k].
+struct SmemLayout {
+  int stages;
+  int stage_bytes;
+  int s_off;        // scales, within a stage
+  int x_off;        // bf16 activations, within a stage
+  int x_box_bytes;  // one activation box
+  int x_tx;         // activation bytes a stage receives
+  int x16_off;      // f16 activation tile, within a stage (f16 path)
+  int exp_off;      // int[8] activation exponents, within a stage (f16 path)
+  int part_off;     // CTA partials [16G][MT*8] f32
+  int lut_off;      // 256 scale pairs
+  int bar_off;      // full[stages], conv[stages], empty[stages], abort flag
+  int total;        // dynamic shared memory to request (includes alignment slack)
 };
+
+__host__ __device__ constexpr int align_up(int v, int a) { return (v + a - 1) / a * a; }
+
+__host__ __device__ constexpr SmemLayout make_layout(int mt, int groups, int stages,
+                                                     bool f16, int m_rows) {
+  SmemLayout l{};
+  const int w_bytes = groups * kGroupRows * (kStageK / 2);
+  const int s_end = w_bytes + groups * kGroupRows * (kStageK / 16);
+  int end = 0;
+  l.stages = stages;
+  l.s_off = w_bytes;
+  if (mt == 1) {
+    l.x_off = align_up(s_end, 128);
+    l.x_box_bytes = m_rows * kStageK * 2;
+    l.x_tx = l.x_box_bytes;
+    l.x16_off = align_up(l.x_off + l.x_box_bytes, 128);
+    l.exp_off = l.x16_off + (f16 ? m_rows * kStageK * 2 : 0);
+    end = l.exp_off + (f16 ? 8 * 4 : 0);
+  } else {
+    l.x_off = align_up(s_end, 1024);
+    l.x_box_bytes = mt * 8 * 128;
+    l.x_tx = kKQuarters * l.x_box_bytes;
+    end = l.x_off + kKQuarters * l.x_box_bytes;
+    l.x16_off = l.exp_off = end;
+  }
+  l.stage_bytes = align_up(end, 1024);
+  l.part_off = stages * l.stage_bytes;
+  l.lut_off = l.part_off + groups * kGroupRows * mt * 8 * 4;
+  l.bar_off = l.lut_off + 256 * 4;
+  l.total = l.bar_off + 3 * stages * 8 + 16 + 1024;
+  return l;
+}
+
+// The cross-warp reduction reuses the ring; it must fit.
+__host__ __device__ constexpr bool layout_ok(const SmemLayout& l, int mt, int groups) {
+  return kKQuarters * groups * kGroupRows * mt * 8 * 4 <= l.stages * l.stage_bytes;
+}
 
 struct Params {
   void* y;              // [M, N] (or [M, N/2] with swiglu), bf16 or f32
   int64_t M, N, K;
-  float global_scale;
+  float out_scale;      // fp32(2^10 / global_scale) (bf16 path), 1 / global_scale (f16)
   int stages_total;     // K / 256
   int split;            // CTAs per cluster along k
   int out_f32;          // 1: write f32 (before the bf16 rounding)
   int swiglu;           // 1: rows [0,N/2) gate, [N/2,N) up, y = silu(g)*u
+  SmemLayout lay;
   unsigned int* err;    // device error word
 };
 
-template <int MT>
-__global__ void __launch_bounds__(kThreads)
+// 2^a as fp32, a in [-126, 127].
+__device__ __forceinline__ float pow2f(int a) { return __int_as_float((a + 127) << 23); }
+
+template <int MT, int G, bool F16>
+__global__ void __launch_bounds__(threads_for(F16), F16 ? 2 : 1)
     smallm_kernel(const __grid_constant__ CUtensorMap tm_w,
                   const __grid_constant__ CUtensorMap tm_s,
                   const __grid_constant__ CUtensorMap tm_x, const Params p) {
-  using L = Layout<MT>;
+  constexpr int kThreads = threads_for(F16);
+  constexpr int RG = groups_per_warp(MT);
+  constexpr int C = MT * 8;
+  constexpr int rows = G * kGroupRows;
+  constexpr int half_rows = rows / 2;
+  static_assert(G >= 1 && G <= max_groups(MT), "row groups per CTA out of range");
+  static_assert(!F16 || MT == 1, "the f16 path serves M <= 8");
+  const SmemLayout& L = p.lay;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint32_t* lut = reinterpret_cast<uint32_t*>(smem + L::kLutOff);
-  float* part = reinterpret_cast<float*>(smem + L::kPartOff);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
-  uint64_t* empty = full + L::kStages;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + L::kStages);
+  uint32_t* lut = reinterpret_cast<uint32_t*>(smem + L.lut_off);
+  float* part = reinterpret_cast<float*>(smem + L.part_off);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bar_off);
+  uint64_t* conv = full + L.stages;
+  uint64_t* empty = conv + L.stages;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + L.stages);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int split = p.split;
@@ -91,21 +167,24 @@ __global__ void __launch_bounds__(kThreads)
   const int st_end = static_cast<int>((int64_t)p.stages_total * (z + 1) / split);
   const int n_stages = st_end - st_begin;
 
-  // weight rows of this CTA: two 32-row boxes
+  // Weight rows of this CTA, as two boxes of 8G rows: consecutive rows, or
+  // (SwiGLU) 8G gate rows and the 8G matching up rows.
   int row0, row1;
   if (p.swiglu) {
-    row0 = blockIdx.x * kHalfRows;                               // gate
-    row1 = static_cast<int>(p.N / 2) + blockIdx.x * kHalfRows;   // up
+    row0 = blockIdx.x * half_rows;
+    row1 = static_cast<int>(p.N / 2) + blockIdx.x * half_rows;
   } else {
-    row0 = blockIdx.x * kRows;
-    row1 = row0 + kHalfRows;
+    row0 = blockIdx.x * rows;
+    row1 = row0 + half_rows;
   }
 
-  for (int i = threadIdx.x; i < 256; i += kThreads) lut[i] = scale_pair_from_e4m3(i);
+  for (int i = threadIdx.x; i < 256; i += kThreads)
+    lut[i] = F16 ? scale_pair_f16_from_e4m3(i) : scale_pair_from_e4m3(i);
   if (threadIdx.x == 0) {
-    for (int s = 0; s < L::kStages; ++s) {
+    for (int s = 0; s < L.stages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kConsumerWarps);
+      mbar_init(&conv[s], 1);
+      mbar_init(&empty[s], kConsumerWarps + (F16 ? 1 : 0));
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -120,120 +199,263 @@ __global__ void __launch_bounds__(kThreads)
       prefetch_tensormap(&tm_x);
       const uint64_t pol_stream = policy_evict_first();
       const uint64_t pol_keep = policy_evict_last();
-      int issued = 0;
-      for (int it = 0; it < n_stages; ++it) {
-        const int slot = it % L::kStages;
-        const uint32_t par = ((it / L::kStages) & 1) ^ 1;
-        if (!mbar_wait(&empty[slot], par, abort_flag)) break;
-        uint8_t* st = smem + slot * L::kStageBytes;
-        mbar_arrive_expect_tx(&full[slot], L::kStageBytes);
+      const uint32_t tx =
+          static_cast<uint32_t>(rows * (kStageK / 2 + kStageK / 16) + L.x_tx);
+      auto issue_weights = [&](int it, int slot) {
+        uint8_t* st = smem + slot * L.stage_bytes;
         const int k0 = (st_begin + it) * kStageK;
         tma_load_2d_hint(st, &tm_w, &full[slot], k0 / 2, row0, pol_stream);
-        tma_load_2d_hint(st + kWBytes / 2, &tm_w, &full[slot], k0 / 2, row1, pol_stream);
-        tma_load_2d_hint(st + kSOff, &tm_s, &full[slot], k0 / 16, row0, pol_stream);
-        tma_load_2d_hint(st + kSOff + kSBytes / 2, &tm_s, &full[slot], k0 / 16, row1,
+        tma_load_2d_hint(st + half_rows * 128, &tm_w, &full[slot], k0 / 2, row1, pol_stream);
+        tma_load_2d_hint(st + L.s_off, &tm_s, &full[slot], k0 / 16, row0, pol_stream);
+        tma_load_2d_hint(st + L.s_off + half_rows * 16, &tm_s, &full[slot], k0 / 16, row1,
                          pol_stream);
+      };
+      auto issue_acts = [&](int it, int slot) {
+        uint8_t* st = smem + slot * L.stage_bytes;
+        const int k0 = (st_begin + it) * kStageK;
+        if (MT == 1) {
+          tma_load_2d_hint(st + L.x_off, &tm_x, &full[slot], k0, 0, pol_keep);
+        } else {
 #pragma unroll
-        for (int q = 0; q < kConsumerWarps; ++q)
-          tma_load_2d_hint(st + kXOff + q * L::kXBoxBytes, &tm_x, &full[slot], k0 + 64 * q,
-                           0, pol_keep);
+          for (int q = 0; q < kKQuarters; ++q)
+            tma_load_2d_hint(st + L.x_off + q * L.x_box_bytes, &tm_x, &full[slot],
+                             k0 + 64 * q, 0, pol_keep);
+        }
+      };
+      // The weights do not depend on the preceding kernel in the stream:
+      // fill the ring with them first, then wait for that kernel before
+      // touching the activations.
+      const int pre = n_stages < L.stages ? n_stages : L.stages;
+      for (int it = 0; it < pre; ++it) {
+        mbar_arrive_expect_tx(&full[it], tx);
+        issue_weights(it, it);
+      }
+      griddep_wait();
+      for (int it = 0; it < pre; ++it) issue_acts(it, it);
+      int issued = pre;
+      for (int it = pre; it < n_stages; ++it) {
+        const int slot = it % L.stages;
+        const uint32_t par = ((it / L.stages) & 1) ^ 1;
+        if (!mbar_wait(&empty[slot], par, abort_flag)) break;
+        mbar_arrive_expect_tx(&full[slot], tx);
+        issue_weights(it, slot);
+        issue_acts(it, slot);
         ++issued;
       }
       // Drain: never leave a copy in flight into this CTA's shared memory.
-      const int first = issued > L::kStages ? issued - L::kStages : 0;
+      const int first = issued > L.stages ? issued - L.stages : 0;
       for (int it = first; it < issued; ++it) {
         volatile int no_abort = 0;
-        if (!mbar_wait(&full[it % L::kStages], (it / L::kStages) & 1, &no_abort))
+        if (!mbar_wait(&full[it % L.stages], (it / L.stages) & 1, &no_abort))
           atomicOr(p.err, kErrWaitTimeout);
       }
     }
-  } else {
-    // ------------------------------------------------------------ consumers
-    const int g = lane >> 2, t = lane & 3;
-    float acc[4][MT][4];
+  } else if (F16 && warp == kConsumerWarps + 1) {
+    // ------------------------------------------------------------ converter
+    // Lane l takes the 16-byte chunk l (8 consecutive k) of every activation
+    // row of every stage.  a_run[m] is row m's exponent: x is stored as
+    // f16(x * 2^a_run), with a_run the largest value keeping the row's
+    // running maximum below 2^15 (so no f16 overflow).
+    const int M = static_cast<int>(p.M);
+    int a_run[kF16MaxRows];
 #pragma unroll
-    for (int r = 0; r < 4; ++r)
+    for (int m = 0; m < kF16MaxRows; ++m) a_run[m] = 126;
+    for (int it = 0; it < n_stages; ++it) {
+      const int slot = it % L.stages;
+      if (!mbar_wait(&full[slot], (it / L.stages) & 1, abort_flag)) break;
+      uint8_t* st = smem + slot * L.stage_bytes;
+#pragma unroll
+      for (int m = 0; m < kF16MaxRows; ++m) {
+        if (m >= M) break;
+        const uint4 v = *reinterpret_cast<const uint4*>(st + L.x_off + m * 512 + lane * 16);
+        uint32_t mx = max_u16x2(max_u16x2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
+                                max_u16x2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
+        mx = __reduce_max_sync(0xffffffffu, max(mx & 0xFFFFu, mx >> 16));
+        const int e_max = static_cast<int>(mx >> 7);         // biased bf16 exponent
+        a_run[m] = min(a_run[m], max(-126, 141 - e_max));    // max * 2^a < 2^15
+        const float f = pow2f(a_run[m]);
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          o[j] = f32x2_to_f16x2(__uint_as_float(w4[j] << 16) * f,
+                                __uint_as_float(w4[j] & 0xFFFF0000u) * f);
+        *reinterpret_cast<uint4*>(st + L.x16_off + m * 512 + ((lane ^ (m & 7)) << 4)) =
+            make_uint4(o[0], o[1], o[2], o[3]);
+        if (lane == 0) reinterpret_cast<int*>(st + L.exp_off)[m] = a_run[m];
+      }
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&conv[slot]);
+        mbar_arrive(&empty[slot]);
+      }
+    }
+  } else if (warp < kConsumerWarps) {
+    // ------------------------------------------------------------ consumers
+    // warp = (k quarter kq, row-group parity rp): 64 k of every stage for
+    // the row groups rp, rp+2, ... of this CTA.
+    const int kq = warp & 3, rp = warp >> 2;
+    const int g = lane >> 2, t = lane & 3;
+    float acc[RG][MT][4];
+#pragma unroll
+    for (int i = 0; i < RG; ++i)
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-        for (int c = 0; c < 4; ++c) acc[r][mt][c] = 0.f;
+        for (int c = 0; c < 4; ++c) acc[i][mt][c] = 0.f;
+    int a_col[2] = {126, 126};            // f16 path: exponents of columns 2t, 2t+1
+
+    // MMA rows g and g+8 of group r are weight rows 16r+2g and 16r+2g+1:
+    // with the 128B swizzle this makes the weight loads bank-conflict free.
+    // Row 16r+2g+h has swizzle phase (2g+h) & 7 for every r, so each load
+    // below is a per-thread base plus a compile-time offset for r.
+    const int chunk = 2 * kq + (t >> 1);
+    int w_base[2], s_base[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int row = kGroupRows * rp + 2 * g + h;
+      w_base[h] = row * 128 + ((chunk ^ (row & 7)) << 4) + ((t & 1) << 3);
+      s_base[h] = L.s_off + row * 16 + 4 * kq + t;
+    }
+    // Activations for MMA column g: elements [16t, 16t+16) of this warp's
+    // 64-k quarter.  bf16: paired (k, k+4) like the bit trick's weights;
+    // f16: the converter's tile, consecutive pairs.  Rows >= M are zero.
+    const bool x_row = MT > 1 || g < static_cast<int>(p.M);
+    int x_off[MT][2];
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      const int m = mt * 8 + g;
+      if (MT == 1 && F16) {
+        const int c = 8 * kq + 2 * t;
+        x_off[mt][0] = L.x16_off + m * 512 + ((c ^ (m & 7)) << 4);
+        x_off[mt][1] = L.x16_off + m * 512 + (((c + 1) ^ (m & 7)) << 4);
+      } else if (MT == 1) {
+        x_off[mt][0] = L.x_off + m * 512 + kq * 128 + t * 32;
+        x_off[mt][1] = x_off[mt][0] + 16;
+      } else {
+        const int box = L.x_off + kq * L.x_box_bytes + m * 128;
+        x_off[mt][0] = box + (((2 * t) ^ (m & 7)) << 4);
+        x_off[mt][1] = box + (((2 * t + 1) ^ (m & 7)) << 4);
+      }
+    }
 
     for (int it = 0; it < n_stages; ++it) {
-      const int slot = it % L::kStages;
-      const uint32_t par = (it / L::kStages) & 1;
+      const int slot = it % L.stages;
+      const uint32_t par = (it / L.stages) & 1;
       if (!mbar_wait(&full[slot], par, abort_flag)) break;
-      const uint8_t* st = smem + slot * L::kStageBytes;
+      if (F16 && !mbar_wait(&conv[slot], par, abort_flag)) break;
+      const uint8_t* st = smem + slot * L.stage_bytes;
 
-      // Activation fragments: x row (8*mt + g), elements [16t, 16t+16) of
-      // this warp's 64-k box, paired (k, k+4) like the weights.
       uint32_t bx[MT][8];
-      const uint8_t* xb = st + kXOff + warp * L::kXBoxBytes;
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) {
-        const int m = mt * 8 + g;
-        const uint8_t* row = xb + m * 128;
-        const uint4 c0 = *reinterpret_cast<const uint4*>(row + (((2 * t) ^ (m & 7)) << 4));
-        const uint4 c1 =
-            *reinterpret_cast<const uint4*>(row + (((2 * t + 1) ^ (m & 7)) << 4));
-        bx[mt][0] = prmt(c0.x, c0.z, 0x5410u);
-        bx[mt][1] = prmt(c0.x, c0.z, 0x7632u);
-        bx[mt][2] = prmt(c0.y, c0.w, 0x5410u);
-        bx[mt][3] = prmt(c0.y, c0.w, 0x7632u);
-        bx[mt][4] = prmt(c1.x, c1.z, 0x5410u);
-        bx[mt][5] = prmt(c1.x, c1.z, 0x7632u);
-        bx[mt][6] = prmt(c1.y, c1.w, 0x5410u);
-        bx[mt][7] = prmt(c1.y, c1.w, 0x7632u);
+        uint4 c0 = make_uint4(0u, 0u, 0u, 0u), c1 = c0;
+        if (x_row) {
+          c0 = *reinterpret_cast<const uint4*>(st + x_off[mt][0]);
+          c1 = *reinterpret_cast<const uint4*>(st + x_off[mt][1]);
+        }
+        if (F16) {
+          bx[mt][0] = c0.x; bx[mt][1] = c0.y; bx[mt][2] = c0.z; bx[mt][3] = c0.w;
+          bx[mt][4] = c1.x; bx[mt][5] = c1.y; bx[mt][6] = c1.z; bx[mt][7] = c1.w;
+        } else {
+          bx[mt][0] = prmt(c0.x, c0.z, 0x5410u);
+          bx[mt][1] = prmt(c0.x, c0.z, 0x7632u);
+          bx[mt][2] = prmt(c0.y, c0.w, 0x5410u);
+          bx[mt][3] = prmt(c0.y, c0.w, 0x7632u);
+          bx[mt][4] = prmt(c1.x, c1.z, 0x5410u);
+          bx[mt][5] = prmt(c1.x, c1.z, 0x7632u);
+          bx[mt][6] = prmt(c1.y, c1.w, 0x5410u);
+          bx[mt][7] = prmt(c1.y, c1.w, 0x7632u);
+        }
+      }
+      if (F16) {
+        // A column's exponent only ever decreases; rescale its running sums
+        // (exactly, by a power of two) when it does.
+        const int2 an = *reinterpret_cast<const int2*>(st + L.exp_off + 8 * t);
+        if (an.x != a_col[0] || an.y != a_col[1]) {
+          const float f0 = pow2f(an.x - a_col[0]), f1 = pow2f(an.y - a_col[1]);
+#pragma unroll
+          for (int i = 0; i < RG; ++i) {
+            acc[i][0][0] *= f0; acc[i][0][2] *= f0;
+            acc[i][0][1] *= f1; acc[i][0][3] *= f1;
+          }
+          a_col[0] = an.x;
+          a_col[1] = an.y;
+        }
       }
 
-      const int chunk = 2 * warp + (t >> 1);
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        // MMA rows g and g+8 are weight rows 16r+2g and 16r+2g+1 (this
-        // choice makes the swizzled loads below bank-conflict free).
-        const int ra = 16 * r + 2 * g, rb = ra + 1;
-        const uint2 wa = *reinterpret_cast<const uint2*>(
-            st + ra * 128 + ((chunk ^ (ra & 7)) << 4) + ((t & 1) << 3));
-        const uint2 wb = *reinterpret_cast<const uint2*>(
-            st + rb * 128 + ((chunk ^ (rb & 7)) << 4) + ((t & 1) << 3));
-        const uint32_t sa = lut[st[kSOff + ra * 16 + 4 * warp + t]];
-        const uint32_t sb = lut[st[kSOff + rb * 16 + 4 * warp + t]];
+      for (int i = 0; i < RG; ++i) {
+        const int r = rp + 2 * i;
+        if (r >= G) break;                       // uniform across the warp
+        const uint2 wa =
+            *reinterpret_cast<const uint2*>(st + w_base[0] + i * 2 * kGroupRows * 128);
+        const uint2 wb =
+            *reinterpret_cast<const uint2*>(st + w_base[1] + i * 2 * kGroupRows * 128);
+        const uint32_t sa = lut[st[s_base[0] + i * 2 * kGroupRows * 16]];
+        const uint32_t sb = lut[st[s_base[1] + i * 2 * kGroupRows * 16]];
         uint32_t pa[8], pb[8];
-        dequant8_strided(wa.x, sa, &pa[0]);
-        dequant8_strided(wa.y, sa, &pa[4]);
-        dequant8_strided(wb.x, sb, &pb[0]);
-        dequant8_strided(wb.y, sb, &pb[4]);
+        if (F16) {
+          dequant8_f16(wa.x, sa, &pa[0]);
+          dequant8_f16(wa.y, sa, &pa[4]);
+          dequant8_f16(wb.x, sb, &pb[0]);
+          dequant8_f16(wb.y, sb, &pb[4]);
+        } else {
+          dequant8_strided(wa.x, sa, &pa[0]);
+          dequant8_strided(wa.y, sa, &pa[4]);
+          dequant8_strided(wb.x, sb, &pb[0]);
+          dequant8_strided(wb.y, sb, &pb[4]);
+        }
 #pragma unroll
         for (int s = 0; s < 4; ++s)
 #pragma unroll
-          for (int mt = 0; mt < MT; ++mt)
-            mma_bf16_16816(acc[r][mt], pa[2 * s], pb[2 * s], pa[2 * s + 1], pb[2 * s + 1],
-                           bx[mt][2 * s], bx[mt][2 * s + 1]);
+          for (int mt = 0; mt < MT; ++mt) {
+            if (F16)
+              mma_f16_16816(acc[i][mt], pa[2 * s], pb[2 * s], pa[2 * s + 1], pb[2 * s + 1],
+                            bx[mt][2 * s], bx[mt][2 * s + 1]);
+            else
+              mma_bf16_16816(acc[i][mt], pa[2 * s], pb[2 * s], pa[2 * s + 1], pb[2 * s + 1],
+                             bx[mt][2 * s], bx[mt][2 * s + 1]);
+          }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[slot]);
     }
+    if (F16) {
+      // back to the activations' own units: divide column c by 2^a_col
+      const float u0 = pow2f(-a_col[0]), u1 = pow2f(-a_col[1]);
+#pragma unroll
+      for (int i = 0; i < RG; ++i) {
+        acc[i][0][0] *= u0;
+        acc[i][0][2] *= u0;
+        acc[i][0][1] *= u1;
+        acc[i][0][3] *= u1;
+      }
+    }
 
     // Warp partials -> ring (free now: every stage has been consumed once
-    // all four warps pass the barrier below).
+    // all consumer warps pass the barrier below).
     asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
     float* red = reinterpret_cast<float*>(smem);
-    constexpr int C = MT * 8;
 #pragma unroll
-    for (int r = 0; r < 4; ++r)
+    for (int i = 0; i < RG; ++i) {
+      const int r = rp + 2 * i;
+      if (r >= G) break;
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) {
-        const int ra = 16 * r + 2 * g, col = mt * 8 + 2 * t;
-        float* base = red + warp * kRows * C;
-        base[ra * C + col] = acc[r][mt][0];
-        base[ra * C + col + 1] = acc[r][mt][1];
-        base[(ra + 1) * C + col] = acc[r][mt][2];
-        base[(ra + 1) * C + col + 1] = acc[r][mt][3];
+        const int ra = kGroupRows * r + 2 * g, col = mt * 8 + 2 * t;
+        float* base = red + kq * rows * C;
+        base[ra * C + col] = acc[i][mt][0];
+        base[ra * C + col + 1] = acc[i][mt][1];
+        base[(ra + 1) * C + col] = acc[i][mt][2];
+        base[(ra + 1) * C + col + 1] = acc[i][mt][3];
       }
+    }
     asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
-    for (int i = threadIdx.x; i < kRows * C; i += kConsumerWarps * 32) {
+    for (int i = threadIdx.x; i < rows * C; i += kConsumerWarps * 32) {
       float s = 0.f;
 #pragma unroll
-      for (int w = 0; w < kConsumerWarps; ++w) s += red[w * kRows * C + i];
+      for (int q = 0; q < kKQuarters; ++q) s += red[q * rows * C + i];
       part[i] = s;
     }
   }
@@ -241,13 +463,19 @@ __global__ void __launch_bounds__(kThreads)
   if (*abort_flag && threadIdx.x == 0) atomicOr(p.err, kErrWaitTimeout);
 
   // ---------------------------------------------------------------- epilogue
+  // The next kernel in the stream may start its prologue now.
+  if (threadIdx.x == 0) griddep_launch_dependents();
   // Every CTA of the cluster finishes its partial; CTA z then reduces a
   // 1/split share of the outputs across the cluster's shared memories.
-  cluster_sync();
+  // (Reconverge each warp first: the cluster barrier is a warp-aligned op.)
+  __syncwarp();
+  if (split > 1)
+    cluster_sync();
+  else
+    __syncthreads();
   {
-    constexpr int C = MT * 8;
     const int M = static_cast<int>(p.M);
-    const int R = p.swiglu ? kHalfRows : kRows;          // outputs per CTA row
+    const int R = p.swiglu ? half_rows : rows;           // outputs per activation row
     const int items = R * M;
     const int i0 = static_cast<int>((int64_t)items * z / split);
     const int i1 = static_cast<int>((int64_t)items * (z + 1) / split);
@@ -256,17 +484,20 @@ __global__ void __launch_bounds__(kThreads)
     const int64_t n_base = static_cast<int64_t>(blockIdx.x) * R;
     for (int i = i0 + threadIdx.x; i < i1; i += kThreads) {
       const int m = i / R, j = i % R;
+      if (n_base + j >= n_out) continue;
       float v = 0.f, u = 0.f;
-      for (int q = 0; q < split; ++q) {
-        const uint32_t base = map_to_rank(part_local, q);
-        v += ld_cluster_f32(base + 4u * (j * C + m));
-        if (p.swiglu) u += ld_cluster_f32(base + 4u * ((kHalfRows + j) * C + m));
+      if (split == 1) {
+        v = part[j * C + m];
+        if (p.swiglu) u = part[(half_rows + j) * C + m];
+      } else {
+        for (int q = 0; q < split; ++q) {
+          const uint32_t base = map_to_rank(part_local, q);
+          v += ld_cluster_f32(base + 4u * (j * C + m));
+          if (p.swiglu) u += ld_cluster_f32(base + 4u * ((half_rows + j) * C + m));
+        }
       }
-      float yv = __fdiv_rn(v * kWeightPow2, p.global_scale);
-      if (p.swiglu) {
-        const float up = __fdiv_rn(u * kWeightPow2, p.global_scale);
-        yv = yv / (1.0f + expf(-yv)) * up;
-      }
+      float yv = v * p.out_scale;
+      if (p.swiglu) yv = silu_mul(yv, u * p.out_scale);
       const int64_t off = static_cast<int64_t>(m) * n_out + n_base + j;
       if (p.out_f32)
         static_cast<float*>(p.y)[off] = yv;
@@ -274,7 +505,10 @@ __global__ void __launch_bounds__(kThreads)
         static_cast<__nv_bfloat16*>(p.y)[off] = __float2bfloat16_rn(yv);
     }
   }
-  cluster_sync();   // keep every partial alive until all readers are done
+  if (split > 1) {
+    __syncwarp();
+    cluster_sync();   // keep every partial alive until all readers are done
+  }
 }
 
 }  // namespace smallm

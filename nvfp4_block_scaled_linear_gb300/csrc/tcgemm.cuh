@@ -56,7 +56,7 @@ static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
 struct Params {
   void* y;
   int64_t M, N, K;
-  float global_scale;
+  float out_scale;      // fp32(2^10 / global_scale)
   int out_f32;
   int swiglu;          // tile = 64 gate rows + the 64 matching up rows
   unsigned int* err;
@@ -118,14 +118,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tensormap(&tm_w);
       prefetch_tensormap(&tm_s);
       const uint64_t pol_w = policy_evict_last();    // weights: reused by M tiles
-      int issued = 0;
-      for (int it = 0; it < n_stages; ++it) {
-        const int slot = it % kStages;
-        if (!mbar_wait(&empty[slot], ((it / kStages) & 1) ^ 1, abort_flag)) break;
+      auto issue_weights = [&](int it, int slot) {
         uint8_t* st = smem + slot * kStageBytes;
         const int k0 = it * kStageK;
-        mbar_arrive_expect_tx(&tma_full[slot], kTxBytes);
-        tma_load_2d(st + kXOff, &tm_x, &tma_full[slot], k0, m_tile);
         tma_load_2d_hint(st + kRawOff, &tm_w, &tma_full[slot], k0 / 2, wrow0, pol_w);
         tma_load_2d_hint(st + kRawOff + kRawBytes / 2, &tm_w, &tma_full[slot], k0 / 2, wrow1,
                          pol_w);
@@ -133,6 +128,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_2d_hint(st + kSclOff, &tm_s, &tma_full[slot], sx, wrow0, pol_w);
         tma_load_2d_hint(st + kSclOff + kSclBytes / 2, &tm_s, &tma_full[slot], sx, wrow1,
                          pol_w);
+      };
+      auto issue_acts = [&](int it, int slot) {
+        tma_load_2d(smem + slot * kStageBytes + kXOff, &tm_x, &tma_full[slot], it * kStageK,
+                    m_tile);
+      };
+      // Weights first (independent of the preceding kernel in the stream),
+      // activations after the programmatic-dependent-launch wait.
+      const int pre = n_stages < kStages ? n_stages : kStages;
+      for (int it = 0; it < pre; ++it) {
+        mbar_arrive_expect_tx(&tma_full[it], kTxBytes);
+        issue_weights(it, it);
+      }
+      griddep_wait();
+      for (int it = 0; it < pre; ++it) issue_acts(it, it);
+      int issued = pre;
+      for (int it = pre; it < n_stages; ++it) {
+        const int slot = it % kStages;
+        if (!mbar_wait(&empty[slot], ((it / kStages) & 1) ^ 1, abort_flag)) break;
+        mbar_arrive_expect_tx(&tma_full[slot], kTxBytes);
+        issue_weights(it, slot);
+        issue_acts(it, slot);
         ++issued;
       }
       const int first = issued > kStages ? issued - kStages : 0;
@@ -201,11 +217,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;                       // TMEM lane quarter
     const int colhalf = d >> 2;                   // activation rows [128c, 128c+128)
-    const bool have_acc = mbar_wait(acc_full, 0, abort_flag);
+    if (warp == 2 && lane == 0) griddep_launch_dependents();
+    // Warp-uniform (and reconverged) before the warp-aligned tcgen05.ld.
+    const bool have_acc = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, abort_flag));
     tc_fence_after_sync();
     if (have_acc) {
       const int lane_row = 32 * q + lane;         // A row = TMEM lane
-      const float inv = kWeightPow2;
       const int64_t n_out = p.swiglu ? p.N / 2 : p.N;
       int64_t ncol;
       if (p.swiglu)
@@ -220,10 +237,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const int m = m_tile + c0 + i;
-          float yv = __fdiv_rn(__uint_as_float(v[i]) * inv, p.global_scale);
+          float yv = __uint_as_float(v[i]) * p.out_scale;
           if (p.swiglu) {
             const float up = __shfl_xor_sync(0xffffffffu, yv, 1);
-            yv = yv / (1.0f + expf(-yv)) * up;
+            yv = silu_mul(yv, up);
             if ((lane & 1) || m >= p.M) continue;
           } else if (m >= p.M) {
             continue;

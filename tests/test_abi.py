@@ -32,6 +32,9 @@ def test_header_constants_match_binding():
                         ("NVFP4_KERNEL_SMALLM", _lib.KERNEL_SMALLM),
                         ("NVFP4_KERNEL_TCGEMM", _lib.KERNEL_TCGEMM)):
         assert "#define %s %du" % (name, value) in text or "#define %s %d " % (name, value) in text
+    assert "#define NVFP4_FLAG_BF16_MMA (1u << 17)" in text and _lib.FLAG_BF16_MMA == 1 << 17
+    assert "#define NVFP4_FLAG_SPLIT_SHIFT 8" in text and _lib.FLAG_SPLIT(3) == 3 << 8
+    assert "#define NVFP4_FLAG_GROUPS_SHIFT 13" in text and _lib.FLAG_GROUPS(5) == 5 << 13
 
 
 def test_version_and_status_strings(lib):
@@ -85,6 +88,11 @@ def test_rejects_before_any_device_work(lib):
     assert _call(lib, A, A, A, A, 0, 256, 512) == 0
     assert _call(lib, None, A, A, None, 0, 256, 512) == 0
     assert _call(lib, None, None, A, None, 0, 256, 512) == -1
+    # tuning overrides out of range
+    assert lib.nvfp4_linear_ex(A, A, A, ctypes.c_float(1.0), A, 1, 256, 512,
+                               _lib.FLAG_SPLIT(17), None) == -1
+    assert lib.nvfp4_linear_ex(A, A, A, ctypes.c_float(1.0), A, 1, 256, 512,
+                               _lib.FLAG_GROUPS(9), None) == -1
 
 
 def test_binding_refuses_cpu_tensors(lib):

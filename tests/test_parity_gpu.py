@@ -8,7 +8,8 @@ import oracle
 from _parity import (check_bf16, check_f32, check_swiglu_bf16, check_swiglu_f32)
 from nvfp4_block_scaled_linear_gb300 import _lib
 from nvfp4_block_scaled_linear_gb300 import build as cuda_build
-from nvfp4_block_scaled_linear_gb300.inputs import (WORKLOADS, LinearInputs, make_linear)
+from nvfp4_block_scaled_linear_gb300.inputs import (WORKLOADS, LinearInputs, draw_linear,
+                                                    make_linear)
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0")
@@ -101,6 +102,126 @@ def test_both_kernels_agree_at_small_m(M):
     t = make_linear(M, 256, 512, seed=500 + M)
     full_check(t, _lib.FLAG_FORCE_TCGEMM, what="forced tcgemm M=%d" % M)
     full_check(t, _lib.FLAG_FORCE_SMALLM, what="forced smallm M=%d" % M)
+
+
+def _oracle(t):
+    y64, a = oracle.linear_f64(t.x_bits, t.w_packed, t.w_scale, t.global_scale)
+    return y64, a
+
+
+def _check_against(t, y64, a, flags, what):
+    y32 = run(t, flags | _lib.FLAG_F32_OUT).cpu().numpy()
+    check_f32(y32, y64, a, what + " f32")
+    ybf = bf16_bits(run(t, flags))
+    check_bf16(ybf, y64, a, oracle.to_bf16_bits(y64), what + " bf16")
+
+
+@pytest.mark.parametrize("M", [1, 7, 16, 32])
+def test_smallm_every_cta_height_and_split(M):
+    """Every CTA height (16*g rows, g = 1..8; ragged row tails where 16*g
+    does not divide N) and k split (one cluster of s CTAs, uneven when s
+    does not divide the K/256 stages) the planner may pick, forced."""
+    N, K = 640, 4096
+    t = make_linear(M, N, K, seed=1000 + M)
+    y64, a = _oracle(t)
+    g_max = 8 if M <= 16 else 4
+    ran = 0
+    for g in range(1, g_max + 1):
+        for s in (1, 2, 3, 5, 8, 16):
+            flags = _lib.FLAG_GROUPS(g) | _lib.FLAG_SPLIT(s)
+            try:
+                _check_against(t, y64, a, flags, "M=%d g=%d split=%d" % (M, g, s))
+                ran += 1
+            except _lib.Nvfp4Error as e:      # a layout that does not fit
+                assert e.status == -1, str(e)
+    assert ran >= 6 * g_max - 4, ran
+
+
+@pytest.mark.parametrize("M", [1, 7, 32])
+def test_smallm_swiglu_overrides(M):
+    t = make_linear(M, 1024, 2048, seed=1100 + M)
+    for g, s in ((1, 1), (2, 3), (4, 8)):
+        full_check(t, _lib.FLAG_SWIGLU | _lib.FLAG_GROUPS(g) | _lib.FLAG_SPLIT(s),
+                   what="swiglu M=%d g=%d split=%d" % (M, g, s))
+
+
+@pytest.mark.parametrize("M", [1, 3, 8])
+def test_smallm_bf16_multiply_path(M):
+    """M <= 8 defaults to f16 operands; the bf16 path is kept as an option
+    and must meet the same bound."""
+    t = make_linear(M, 384, 2048, seed=1200 + M)
+    full_check(t, _lib.FLAG_BF16_MMA, what="bf16-mma M=%d" % M)
+    full_check(t, 0, what="f16 M=%d" % M)
+
+
+def _wide_range_inputs(M, seed):
+    """Activation rows that stress the f16 path's per-row power-of-two
+    scaling: magnitudes spread over 2^-40..2^20 in one row, a row whose
+    large values arrive only in the last k stages (the running maximum
+    grows mid-row), a row scaled by 2^-60, and a sparse row of values near
+    3e5 (beyond f16's range before scaling)."""
+    rng = np.random.default_rng(seed)
+    N, K = 256, 2048
+    x = rng.standard_normal((M, K)).astype(np.float32)
+    x[0] = np.sign(rng.standard_normal(K)) * np.exp2(rng.uniform(-40, 20, K))
+    if M > 1:
+        x[1] *= np.float32(1e-3)
+        x[1, -300:] = rng.standard_normal(300).astype(np.float32) * np.float32(4e4)
+    if M > 2:
+        x[2] *= np.float32(2.0 ** -60)
+    if M > 3:
+        x[3] = 0.0
+        idx = rng.choice(K, 12, replace=False)
+        x[3, idx] = rng.uniform(2.5e5, 3.5e5, 12).astype(np.float32) * np.sign(
+            rng.standard_normal(12)).astype(np.float32)
+    wp = rng.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    ws = rng.integers(0x20, 0x51, size=(N, K // 16), dtype=np.uint8)
+    from nvfp4_block_scaled_linear_gb300.inputs import GLOBAL_SCALE, f32_to_bf16_bits
+    return LinearInputs(f32_to_bf16_bits(x), wp, ws, GLOBAL_SCALE)
+
+
+@pytest.mark.parametrize("M,flags", [(4, 0), (8, 0), (4, _lib.FLAG_BF16_MMA), (12, 0),
+                                     (40, 0)])
+def test_wide_dynamic_range_rows(M, flags):
+    t = _wide_range_inputs(M, seed=1300 + M)
+    y64, a = _oracle(t)
+    _check_against(t, y64, a, flags, "wide-range M=%d flags=%d" % (M, flags))
+    # the row scaled by 2^-60 is held to the relative bound alone (the
+    # absolute 1e-6 would make its check vacuous)
+    y32 = run(t, flags | _lib.FLAG_F32_OUT).cpu().numpy().astype(np.float64)
+    err = np.abs(y32[2] - y64[2])
+    assert np.all(err <= 1e-4 * a[2]), float(np.max(err / a[2]))
+    assert np.all(np.abs(y64[2]) > 0) and np.all(np.abs(y32[2]) < 2.0 ** -40)
+
+
+@pytest.mark.parametrize("M,flags", [(1, 0), (6, 0), (6, _lib.FLAG_BF16_MMA), (20, 0),
+                                     (6, _lib.FLAG_FORCE_TCGEMM), (50, 0)])
+def test_non_finite_values_propagate(M, flags):
+    """An inf or NaN activation, or a NaN block scale (e4m3 S.1111.111),
+    gives the non-finite outputs the exact sum gives (IEEE: inf * 0 = NaN,
+    inf - inf = NaN); every other output is unaffected."""
+    t = make_linear(M, 256, 1024, seed=1400 + M)
+    x = t.x_bits.copy()
+    x[0, 37] = 0x7F80                         # +inf
+    if M > 2:
+        x[2, 600] = 0xFF80                    # -inf
+        x[M - 1, 5] = 0x7FC0                  # NaN
+    ws = t.w_scale.copy()
+    ws[17, 3] = 0x7F                          # NaN scale: row 17, k in [48, 64)
+    ws[200, 60] = 0xFF
+    t = LinearInputs(x, t.w_packed, ws, t.global_scale)
+    y64, a = _oracle(t)
+    y32 = run(t, flags | _lib.FLAG_F32_OUT).cpu().numpy().astype(np.float64)
+    fin = np.isfinite(y64)
+    assert (~fin).any() and fin.any()
+    assert np.array_equal(np.isnan(y32), np.isnan(y64))
+    assert np.array_equal(y32[np.isinf(y64)], y64[np.isinf(y64)])
+    check_f32(y32[fin], y64[fin], a[fin], "non-finite M=%d" % M)
+    ybf = bf16_bits(run(t, flags))
+    check_bf16(ybf[fin], y64[fin], a[fin], oracle.to_bf16_bits(y64[fin]), "non-finite bf16")
+    vb = oracle.to_bf16_bits(y64)
+    assert np.array_equal(ybf[np.isinf(y64)], vb[np.isinf(y64)])
+    assert np.all((ybf[np.isnan(y64)] & 0x7FFF) > 0x7F80)
 
 
 # ------------------------------------------------------------------ exactness
@@ -222,6 +343,75 @@ def test_repeated_calls_are_deterministic():
     a = bf16_bits(run(t))
     for _ in range(3):
         assert np.array_equal(bf16_bits(run(t)), a)
+
+
+def test_cuda_graph_capture_and_replay():
+    """Calls captured into a CUDA graph (both kernels, SwiGLU and plain)
+    give on replay what the same calls give eagerly, bit for bit, also after
+    the inputs are overwritten in place between replays."""
+    shapes = [(1, 512, 1024, 0), (7, 384, 2048, 0), (32, 512, 1024, _lib.FLAG_SWIGLU),
+              (100, 256, 1024, 0)]
+    ts = [make_linear(M, N, K, seed=1500 + i) for i, (M, N, K, _) in enumerate(shapes)]
+    devs = [to_dev(t) for t in ts]
+    outs = [torch.empty((M, N // 2 if f else N), dtype=torch.bfloat16, device=DEV)
+            for (M, N, K, f) in shapes]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for (x, wp, ws), t, o, (_, _, _, f) in zip(devs, ts, outs, shapes):   # warm-up
+            _lib.linear_ex(x, wp, ws, float(t.global_scale), f, out=o, stream=s)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        st = torch.cuda.current_stream()
+        for (x, wp, ws), t, o, (_, _, _, f) in zip(devs, ts, outs, shapes):
+            _lib.linear_ex(x, wp, ws, float(t.global_scale), f, out=o, stream=st)
+    for rep in range(2):
+        if rep:
+            for (x, _, _) in devs:
+                x.mul_(-2.0)
+        for o in outs:
+            o.fill_(7.0)
+        g.replay()
+        torch.cuda.synchronize()
+        for (x, wp, ws), t, o, (_, _, _, f) in zip(devs, ts, outs, shapes):
+            ref = _lib.linear_ex(x, wp, ws, float(t.global_scale), f)
+            torch.cuda.synchronize()
+            assert torch.equal(o.view(torch.int16), ref.view(torch.int16))
+    # and the eager result is the oracle's
+    t0 = LinearInputs(devs[1][0].cpu().view(torch.int16).numpy().view(np.uint16),
+                      ts[1].w_packed, ts[1].w_scale, ts[1].global_scale)
+    y64, a = _oracle(t0)
+    check_bf16(bf16_bits(outs[1]), y64, a, oracle.to_bf16_bits(y64), "graph replay")
+
+
+@pytest.mark.parametrize("M", [1, 8, 32, 64])
+def test_chained_calls_read_the_previous_output(M):
+    """y1 = L1(x); y2 = L2(y1); y3 = L3(y2) back to back on one stream: each
+    call's activations are the previous call's output, written by the kernel
+    just before it (the calls overlap their weight prefetch with it).  Equal,
+    bit for bit, to the same calls separated by synchronisation."""
+    K0 = 1024
+    dims = [(512, K0), (768, 512), (256, 768)]
+    rng = np.random.default_rng(1600 + M)
+    layers = []
+    for i, (N, K) in enumerate(dims):
+        t = draw_linear(rng, 1, N, K)
+        layers.append((torch.from_numpy(t.w_packed).to(DEV),
+                       torch.from_numpy(t.w_scale).to(DEV), float(t.global_scale)))
+    x = torch.from_numpy(make_linear(M, 128, K0, seed=1700 + M).x_bits.view(np.int16)).view(
+        torch.bfloat16).to(DEV)
+    for _ in range(3):
+        h = x
+        for wp, ws, gs in layers:
+            h = _lib.linear(h, wp, ws, gs)
+        chained = h.clone()
+        h = x
+        for wp, ws, gs in layers:
+            h = _lib.linear(h, wp, ws, gs)
+            torch.cuda.synchronize()
+        assert torch.equal(chained.view(torch.int16), h.view(torch.int16))
 
 
 # ------------------------------------------------------------------ full size
