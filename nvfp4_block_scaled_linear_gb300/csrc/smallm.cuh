@@ -284,6 +284,8 @@ __global__ void __launch_bounds__(threads_for(F16), F16 ? 2 : 1)
             make_uint4(o[0], o[1], o[2], o[3]);
         if (lane == 0) reinterpret_cast<int*>(st + L.exp_off)[m] = a_run[m];
       }
+      // rows past M: a fixed exponent (their columns hold zeros)
+      if (lane >= M && lane < kF16MaxRows) reinterpret_cast<int*>(st + L.exp_off)[lane] = 126;
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&conv[slot]);
@@ -371,13 +373,20 @@ __global__ void __launch_bounds__(threads_for(F16), F16 ? 2 : 1)
       if (F16) {
         // A column's exponent only ever decreases; rescale its running sums
         // (exactly, by a power of two) when it does.
+        // The drop d lies in [-252, 0]: apply 2^d as two factors, each a
+        // normal fp32 power of two, so that the product underflows as the
+        // exact one would (one factor 2^d is not representable below -126).
         const int2 an = *reinterpret_cast<const int2*>(st + L.exp_off + 8 * t);
         if (an.x != a_col[0] || an.y != a_col[1]) {
-          const float f0 = pow2f(an.x - a_col[0]), f1 = pow2f(an.y - a_col[1]);
+          const int d0 = an.x - a_col[0], d1 = an.y - a_col[1];
+          const float f0a = pow2f(d0 >> 1), f0b = pow2f(d0 - (d0 >> 1));
+          const float f1a = pow2f(d1 >> 1), f1b = pow2f(d1 - (d1 >> 1));
 #pragma unroll
           for (int i = 0; i < RG; ++i) {
-            acc[i][0][0] *= f0; acc[i][0][2] *= f0;
-            acc[i][0][1] *= f1; acc[i][0][3] *= f1;
+            acc[i][0][0] = acc[i][0][0] * f0a * f0b;
+            acc[i][0][2] = acc[i][0][2] * f0a * f0b;
+            acc[i][0][1] = acc[i][0][1] * f1a * f1b;
+            acc[i][0][3] = acc[i][0][3] * f1a * f1b;
           }
           a_col[0] = an.x;
           a_col[1] = an.y;

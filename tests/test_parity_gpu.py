@@ -181,7 +181,8 @@ def _wide_range_inputs(M, seed):
 
 
 @pytest.mark.parametrize("M,flags", [(4, 0), (8, 0), (4, _lib.FLAG_BF16_MMA), (12, 0),
-                                     (40, 0)])
+                                     (40, 0), (4, _lib.FLAG_SPLIT(1)), (4, _lib.FLAG_SPLIT(8)),
+                                     (8, _lib.FLAG_SPLIT(3))])
 def test_wide_dynamic_range_rows(M, flags):
     t = _wide_range_inputs(M, seed=1300 + M)
     y64, a = _oracle(t)
@@ -202,7 +203,8 @@ def test_non_finite_values_propagate(M, flags):
     inf - inf = NaN); every other output is unaffected."""
     t = make_linear(M, 256, 1024, seed=1400 + M)
     x = t.x_bits.copy()
-    x[0, 37] = 0x7F80                         # +inf
+    if M > 1:
+        x[0, 37] = 0x7F80                     # +inf (a whole output row non-finite)
     if M > 2:
         x[2, 600] = 0xFF80                    # -inf
         x[M - 1, 5] = 0x7FC0                  # NaN
