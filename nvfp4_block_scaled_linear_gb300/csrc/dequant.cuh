@@ -114,12 +114,21 @@ __device__ __forceinline__ void pair_consecutive(const uint32_t* p, uint32_t* ou
 
 // Eight codes (one 32-bit word, k = 0..7 in order) times the f16 pair scale
 // S -> four f16x2 words of consecutive k: out[j] = (w(2j), w(2j+1)), each
-// w = code * scale exactly.
+// w = code * scale exactly.  The word is split into byte registers, so each
+// conversion reads its byte in place (no shifts).
 __device__ __forceinline__ void dequant8_f16(uint32_t w, uint32_t S, uint32_t* out) {
-  out[0] = f16x2_mul(cvt_e2m1x2_f16x2(w), S);
-  out[1] = f16x2_mul(cvt_e2m1x2_f16x2(w >> 8), S);
-  out[2] = f16x2_mul(cvt_e2m1x2_f16x2(w >> 16), S);
-  out[3] = f16x2_mul(cvt_e2m1x2_f16x2(w >> 24), S);
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t.reg .b32 h0, h1, h2, h3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 h0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 h1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 h2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 h3, b3;\n\t"
+      "mul.rn.f16x2 %0, h0, %5;\n\t"
+      "mul.rn.f16x2 %1, h1, %5;\n\t"
+      "mul.rn.f16x2 %2, h2, %5;\n\t"
+      "mul.rn.f16x2 %3, h3, %5;\n\t}"
+      : "=r"(out[0]), "=r"(out[1]), "=r"(out[2]), "=r"(out[3])
+      : "r"(w), "r"(S));
 }
 
 }  // namespace nvfp4

@@ -198,18 +198,6 @@ __device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Two FP4 e2m1 codes (the low byte of `byte`; low nibble -> low half) to
-// f16x2, exactly (hardware conversion).
-__device__ __forceinline__ uint32_t cvt_e2m1x2_f16x2(uint32_t byte) {
-  uint32_t d;
-  asm("{\n\t.reg .b8 b;\n\t"
-      "cvt.u8.u32 b, %1;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %0, b;\n\t}"
-      : "=r"(d)
-      : "r"(byte));
-  return d;
-}
-
 __device__ __forceinline__ uint32_t f16x2_mul(uint32_t a, uint32_t b) {
   uint32_t d;
   asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));

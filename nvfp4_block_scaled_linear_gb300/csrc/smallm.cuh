@@ -137,6 +137,16 @@ struct Params {
 // 2^a as fp32, a in [-126, 127].
 __device__ __forceinline__ float pow2f(int a) { return __int_as_float((a + 127) << 23); }
 
+// Next position in a ring of `stages` slots; flips the barrier parity on
+// wrap-around.
+__device__ __forceinline__ int next_slot(int slot, int stages, uint32_t& parity) {
+  if (++slot == stages) {
+    parity ^= 1u;
+    return 0;
+  }
+  return slot;
+}
+
 template <int MT, int G, bool F16>
 __global__ void __launch_bounds__(threads_for(F16), F16 ? 2 : 1)
     smallm_kernel(const __grid_constant__ CUtensorMap tm_w,
@@ -190,6 +200,11 @@ __global__ void __launch_bounds__(threads_for(F16), F16 ? 2 : 1)
     fence_mbar_init();
   }
   __syncthreads();
+  // Let the next kernel in the stream launch now: its CTAs take the SM room
+  // this grid leaves free and prefetch their weights while this one runs.
+  // (They read this kernel's results only after griddepcontrol.wait, which
+  // waits for the whole grid to complete.)
+  if (threadIdx.x == 0) griddep_launch_dependents();
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
@@ -233,14 +248,15 @@ __global__ void __launch_bounds__(threads_for(F16), F16 ? 2 : 1)
       griddep_wait();
       for (int it = 0; it < pre; ++it) issue_acts(it, it);
       int issued = pre;
+      int slot = pre == L.stages ? 0 : pre;
+      uint32_t par = pre == L.stages ? 0u : 1u;
       for (int it = pre; it < n_stages; ++it) {
-        const int slot = it % L.stages;
-        const uint32_t par = ((it / L.stages) & 1) ^ 1;
         if (!mbar_wait(&empty[slot], par, abort_flag)) break;
         mbar_arrive_expect_tx(&full[slot], tx);
         issue_weights(it, slot);
         issue_acts(it, slot);
         ++issued;
+        slot = next_slot(slot, L.stages, par);
       }
       // Drain: never leave a copy in flight into this CTA's shared memory.
       const int first = issued > L.stages ? issued - L.stages : 0;
@@ -260,9 +276,10 @@ __global__ void __launch_bounds__(threads_for(F16), F16 ? 2 : 1)
     int a_run[kF16MaxRows];
 #pragma unroll
     for (int m = 0; m < kF16MaxRows; ++m) a_run[m] = 126;
-    for (int it = 0; it < n_stages; ++it) {
-      const int slot = it % L.stages;
-      if (!mbar_wait(&full[slot], (it / L.stages) & 1, abort_flag)) break;
+    int slot = 0;                 // ring position, stepped without a divide
+    uint32_t par = 0;
+    for (int it = 0; it < n_stages; ++it, slot = next_slot(slot, L.stages, par)) {
+      if (!mbar_wait(&full[slot], par, abort_flag)) break;
       uint8_t* st = smem + slot * L.stage_bytes;
 #pragma unroll
       for (int m = 0; m < kF16MaxRows; ++m) {
@@ -341,9 +358,9 @@ __global__ void __launch_bounds__(threads_for(F16), F16 ? 2 : 1)
       }
     }
 
-    for (int it = 0; it < n_stages; ++it) {
-      const int slot = it % L.stages;
-      const uint32_t par = (it / L.stages) & 1;
+    int slot = 0;
+    uint32_t par = 0;
+    for (int it = 0; it < n_stages; ++it, slot = next_slot(slot, L.stages, par)) {
       if (!mbar_wait(&full[slot], par, abort_flag)) break;
       if (F16 && !mbar_wait(&conv[slot], par, abort_flag)) break;
       const uint8_t* st = smem + slot * L.stage_bytes;
@@ -472,8 +489,6 @@ __global__ void __launch_bounds__(threads_for(F16), F16 ? 2 : 1)
   if (*abort_flag && threadIdx.x == 0) atomicOr(p.err, kErrWaitTimeout);
 
   // ---------------------------------------------------------------- epilogue
-  // The next kernel in the stream may start its prologue now.
-  if (threadIdx.x == 0) griddep_launch_dependents();
   // Every CTA of the cluster finishes its partial; CTA z then reduces a
   // 1/split share of the outputs across the cluster's shared memories.
   // (Reconverge each warp first: the cluster barrier is a warp-aligned op.)
