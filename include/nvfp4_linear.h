@@ -66,32 +66,39 @@ extern "C" {
 /* Flags of nvfp4_linear_ex. */
 #define NVFP4_FLAG_SWIGLU 1u        /* fused gate/up: y = silu(gate) * up */
 #define NVFP4_FLAG_F32_OUT 2u       /* write fp32 (before bf16 rounding) */
-#define NVFP4_FLAG_FORCE_SMALLM 4u  /* force the few-row kernel (needs M <= 32) */
+#define NVFP4_FLAG_FORCE_SMALLM 4u  /* force the warp-MMA few-row kernel (needs M <= 32) */
 #define NVFP4_FLAG_FORCE_TCGEMM 8u  /* force the tcgen05 tensor-core kernel */
-/* Tuning override of the few-row kernel: split k over n CTAs of one
- * thread-block cluster (1 <= n <= 16) instead of the built-in choice;
- * n = 0 means automatic.  Encode with NVFP4_FLAG_SPLIT(n). */
+/* Tuning override of both few-row kernels: split k over n CTAs of one
+ * thread-block cluster (1 <= n <= 16, at most K/256) instead of the
+ * built-in choice; n = 0 means automatic.  Encode with NVFP4_FLAG_SPLIT(n). */
 #define NVFP4_FLAG_SPLIT_SHIFT 8
 #define NVFP4_FLAG_SPLIT_MASK (0x1Fu << NVFP4_FLAG_SPLIT_SHIFT)
 #define NVFP4_FLAG_SPLIT(n) (((unsigned int)(n) & 0x1Fu) << NVFP4_FLAG_SPLIT_SHIFT)
-/* Tuning override of the few-row kernel: CTAs of 16 * n weight rows
- * (1 <= n <= 8, at most 4 when M > 16) instead of the built-in choice;
- * n = 0 means automatic.  A combination that does not fit on the device is
- * rejected with NVFP4_ERR_INVALID. */
+/* Tuning override of the warp-MMA few-row kernel: CTAs of 16 * n weight
+ * rows (1 <= n <= 8, at most 4 when M > 16) instead of the built-in
+ * choice; n = 0 means automatic.  A combination that does not fit on the
+ * device is rejected with NVFP4_ERR_INVALID. */
 #define NVFP4_FLAG_GROUPS_SHIFT 13
 #define NVFP4_FLAG_GROUPS_MASK (0xFu << NVFP4_FLAG_GROUPS_SHIFT)
 #define NVFP4_FLAG_GROUPS(n) (((unsigned int)(n) & 0xFu) << NVFP4_FLAG_GROUPS_SHIFT)
-/* Few-row kernel with M <= 8: multiply in bf16, the activations as given,
- * instead of the default f16 path.  The f16 path converts each activation
- * row to f16 after scaling it by a power of two taken from the row's
- * running maximum |x|; it is exact for every activation within a factor
- * 2^31 of that maximum and otherwise rounds it like an f16 subnormal. */
+/* The warp-MMA few-row kernel multiplying in bf16, the activations as
+ * given (exact for any activations; M <= 32).  Without it, both few-row
+ * kernels multiply in f16: code * scale is exact in f16, and each
+ * activation row is brought to f16 after scaling by a power of two taken
+ * from the row's maximum |x| (the warp-MMA kernel: running maximum; the
+ * tcgen05 kernel: maximum within each 256-k stage), which is exact for
+ * every activation within a factor 2^31 of that maximum and otherwise
+ * rounds it like an f16 subnormal.  (The warp-MMA kernel uses f16 only for
+ * M <= 8.) */
 #define NVFP4_FLAG_BF16_MMA (1u << 17)
+/* Force the tcgen05 few-row kernel (needs M <= 32; the default there). */
+#define NVFP4_FLAG_FORCE_GEMV (1u << 18)
 
 /* Kernel identifiers returned by nvfp4_linear_kernel_for. */
 #define NVFP4_KERNEL_NONE 0
-#define NVFP4_KERNEL_SMALLM 1       /* M <= 32: weight-streaming, register-fed MMA */
+#define NVFP4_KERNEL_SMALLM 1       /* few rows, register-fed warp MMA (forced, or bf16) */
 #define NVFP4_KERNEL_TCGEMM 2       /* M > 32: tcgen05 / TMEM tensor-core GEMM */
+#define NVFP4_KERNEL_GEMV 3         /* M <= 32: weight streaming, dequantised into TMEM, tcgen05 */
 
 /* Version of this ABI (NVFP4_ABI_VERSION). */
 int nvfp4_abi_version(void);

@@ -20,6 +20,7 @@ FLAG_F32_OUT = 2
 FLAG_FORCE_SMALLM = 4
 FLAG_FORCE_TCGEMM = 8
 FLAG_BF16_MMA = 1 << 17
+FLAG_FORCE_GEMV = 1 << 18
 
 
 def FLAG_SPLIT(n):
@@ -32,8 +33,8 @@ def FLAG_GROUPS(n):
     return (int(n) & 0xF) << 13
 
 
-KERNEL_NONE, KERNEL_SMALLM, KERNEL_TCGEMM = 0, 1, 2
-KERNEL_NAMES = {KERNEL_SMALLM: "smallm", KERNEL_TCGEMM: "tcgemm"}
+KERNEL_NONE, KERNEL_SMALLM, KERNEL_TCGEMM, KERNEL_GEMV = 0, 1, 2, 3
+KERNEL_NAMES = {KERNEL_SMALLM: "smallm", KERNEL_TCGEMM: "tcgemm", KERNEL_GEMV: "gemv_tc"}
 
 HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
                       "include", "nvfp4_linear.h")

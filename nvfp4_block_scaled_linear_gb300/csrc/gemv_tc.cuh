@@ -1,0 +1,506 @@
+// gemv_tc.cuh -- NVFP4 W4A16 linear for few activation rows (M <= 32):
+// decode (M = 1), speculative verify (M = K+1, FlashRT docs section 3) and
+// small continuous batches, on the tcgen05 tensor cores.
+//
+// At these sizes the layer is bound by streaming the packed weights and
+// scales from HBM once.  What limits a kernel that keeps up with HBM is the
+// instruction issue of the streaming multiprocessors: decoding 16 FP4 codes
+// and applying their block scale costs a few instructions per weight, and
+// register-fed warp MMAs add their own operand traffic on top.  Here the
+// CUDA cores only dequantise; the tensor core does every multiply-add:
+//
+//  * One CTA owns 128 weight rows (the MMA's M; SwiGLU: 64 gate rows and
+//    the 64 matching up rows) and a contiguous range of k.  A producer warp
+//    streams 256-k stages -- packed codes (128B-swizzled), block scales and
+//    the M activation rows -- into a shared-memory ring with TMA.  The codes
+//    of the first ring-full are requested before the kernel waits on the
+//    preceding kernel in the stream (programmatic dependent launch).
+//  * Eight dequantisation warps turn the codes into f16 weights: the
+//    hardware e2m1 -> f16x2 conversion and one f16x2 multiply by the block
+//    scale give code * scale exactly.  Each thread owns one weight row (its
+//    TMEM lane) and writes 64 k of it per half stage straight into tensor
+//    memory with tcgen05.st: the weights never pass through shared memory.
+//  * One thread issues tcgen05.mma kind::f16 with A = the dequantised
+//    weights in TMEM, B = the activations (f16, 128B-swizzled K-major in
+//    shared memory, N = 16 or 32 rows) and D = fp32 in TMEM: 16 MMAs of
+//    K = 16 per stage.
+//  * Two converter warps bring each stage's activation rows to f16 with a
+//    power-of-two scale per row and stage, taken from that row's maximum
+//    |x| within the stage (so the largest value stays below 2^15).  Every
+//    activation within 2^31 of that maximum converts exactly, and nothing
+//    overflows.  Because the scale differs per stage, each stage
+//    accumulates into a fresh D (double-buffered in TMEM), and four
+//    accumulator warps add D * 2^-scale into fp32 registers per row.
+//  * Split-K: CTAs that share rows but not k form one thread-block cluster;
+//    partials are reduced across the cluster through distributed shared
+//    memory.  No global workspace, no atomics, no waits on other CTAs.
+#pragma once
+#include <cstdint>
+#include <cuda_bf16.h>
+
+#include "dequant.cuh"
+#include "ptx.cuh"
+
+namespace nvfp4 {
+namespace gemvtc {
+
+constexpr int kRows = 128;              // weight rows per CTA (the MMA's M)
+constexpr int kHalfRows = kRows / 2;    // one TMA box of rows
+constexpr int kStageK = 256;            // k per pipeline stage
+constexpr int kASlots = 3;              // TMEM weight ring, 128 k (64 columns) each
+constexpr int kAColsPerSlot = 64;
+constexpr int kDCol = kASlots * kAColsPerSlot;   // D buffers start at column 192
+constexpr uint32_t kTmemCols = 256;
+constexpr int kMaxRows = 32;            // activation rows served
+constexpr int kMaxSplit = 16;           // cluster size limit (non-portable above 8)
+
+constexpr int kWarpProducer = 0;
+constexpr int kWarpMma = 1;
+constexpr int kWarpConv = 2;            // two converter warps: 2, 3
+constexpr int kConvWarps = 2;
+constexpr int kWarpDeq = 4;             // eight dequantisation warps: 4..11
+constexpr int kDeqWarps = 8;
+constexpr int kWarpAcc = 12;            // four accumulator warps: 12..15
+constexpr int kAccWarps = 4;
+constexpr int kThreads = (kWarpAcc + kAccWarps) * 32;   // 512
+
+__host__ __device__ constexpr int align_up(int v, int a) { return (v + a - 1) / a * a; }
+
+// Shared-memory layout of one launch (byte offsets from the 1024-aligned
+// base), computed on the host per call.  A stage holds the codes
+// [128 rows][128 B] (128B-swizzled), the scales [128 rows][16 B], the bf16
+// activations [M rows][256 k] and their f16 MMA operand: four 64-k column
+// blocks of [N rows][128 B], 128B-swizzled, N = 16 or 32.
+struct SmemLayout {
+  int stages;
+  int stage_bytes;
+  int s_off;        // scales, within a stage
+  int x_off;        // bf16 activations, within a stage
+  int b_off;        // f16 MMA operand, within a stage
+  int exp_off;      // int[2 * stages][32]: activation exponents per stage
+  int lut_off;      // 256 f16 scale pairs
+  int bar_off;      // mbarriers, abort flag, TMEM base
+  int total;        // dynamic shared memory to request (with alignment slack)
+};
+
+__host__ __device__ constexpr int num_barriers(int stages) { return 5 * stages + 11; }
+
+__host__ __device__ constexpr SmemLayout make_layout(int n_mma, int m_rows, int stages) {
+  SmemLayout l{};
+  l.stages = stages;
+  l.s_off = kRows * 128;
+  l.x_off = align_up(l.s_off + kRows * 16, 128);
+  l.b_off = align_up(l.x_off + m_rows * kStageK * 2, 1024);
+  l.stage_bytes = align_up(l.b_off + n_mma * kStageK * 2, 1024);
+  l.exp_off = stages * l.stage_bytes;
+  l.lut_off = l.exp_off + 2 * stages * kMaxRows * 4;
+  l.bar_off = l.lut_off + 256 * 4;
+  l.total = l.bar_off + num_barriers(stages) * 8 + 16 + 1024;
+  return l;
+}
+
+// The final cross-warp exchange reuses the ring; it must fit.
+__host__ __device__ constexpr bool layout_ok(const SmemLayout& l, int n_mma) {
+  return l.stages >= 2 && kRows * n_mma * 4 <= l.stages * l.stage_bytes;
+}
+
+struct Params {
+  void* y;              // [M, N] (or [M, N/2] with swiglu), bf16 or f32
+  int64_t M, N, K;
+  float out_scale;      // 1 / global_scale
+  int stages_total;     // K / 256
+  int split;            // CTAs per cluster along k
+  int out_f32;          // 1: write f32 (before the bf16 rounding)
+  int swiglu;           // 1: rows [0,N/2) gate, [N/2,N) up, y = silu(g)*u
+  SmemLayout lay;
+  unsigned int* err;    // device error word
+};
+
+__device__ __forceinline__ float pow2f(int a) { return __int_as_float((a + 127) << 23); }
+
+// A wait whose outcome the whole warp shares: the warp-aligned tcgen05 and
+// reduction instructions after it need every lane converged.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity,
+                                          volatile int* abort_flag) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag));
+}
+
+__device__ __forceinline__ int next_slot(int slot, int n, uint32_t& parity) {
+  if (++slot == n) {
+    parity ^= 1u;
+    return 0;
+  }
+  return slot;
+}
+
+template <int NM>
+__global__ void __launch_bounds__(kThreads, NM == 16 ? 2 : 1)
+    gemv_tc_kernel(const __grid_constant__ CUtensorMap tm_w,
+                   const __grid_constant__ CUtensorMap tm_s,
+                   const __grid_constant__ CUtensorMap tm_x, const Params p) {
+  static_assert(NM == 16 || NM == 32, "MMA N is 16 or 32");
+  const SmemLayout& L = p.lay;
+  const int S = L.stages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint32_t* lut = reinterpret_cast<uint32_t*>(smem + L.lut_off);
+  int* exps = reinterpret_cast<int*>(smem + L.exp_off);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bar_off);   // TMA landed
+  uint64_t* empty = full + S;          // stage consumed (MMA commit)
+  uint64_t* b_full = empty + S;        // f16 activations written (converters)
+  uint64_t* exp_full = b_full + S;     // [2S] exponents written (converters)
+  uint64_t* a_full = exp_full + 2 * S; // [3] TMEM weights written (dequantisers)
+  uint64_t* a_empty = a_full + kASlots;    // [3] TMEM weights consumed (MMA commit)
+  uint64_t* d_full = a_empty + kASlots;    // [2] stage accumulator ready (MMA commit)
+  uint64_t* d_empty = d_full + 2;          // [2] stage accumulator read (acc warps)
+  uint64_t* mma_done = d_empty + 2;        // every MMA issued has completed
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(mma_done + 1);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1) + 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int M = static_cast<int>(p.M);
+  const int split = p.split;
+  const int z = blockIdx.y;                                  // k-slice index
+  const int st_begin = static_cast<int>((int64_t)p.stages_total * z / split);
+  const int st_end = static_cast<int>((int64_t)p.stages_total * (z + 1) / split);
+  const int n_stages = st_end - st_begin;
+
+  // Weight rows of this CTA, as two boxes of 64 rows: consecutive rows, or
+  // (SwiGLU) 64 gate rows and the 64 matching up rows.
+  int row0, row1;
+  if (p.swiglu) {
+    row0 = blockIdx.x * kHalfRows;
+    row1 = static_cast<int>(p.N / 2) + blockIdx.x * kHalfRows;
+  } else {
+    row0 = blockIdx.x * kRows;
+    row1 = row0 + kHalfRows;
+  }
+
+  for (int i = threadIdx.x; i < 256; i += kThreads) lut[i] = scale_pair_f16_from_e4m3(i);
+  // The f16 operand rows past M stay zero for the whole launch.
+  for (int s = 0; s < S; ++s) {
+    uint4* b = reinterpret_cast<uint4*>(smem + s * L.stage_bytes + L.b_off);
+    for (int i = threadIdx.x; i < NM * kStageK * 2 / 16; i += kThreads)
+      b[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+      mbar_init(&b_full[s], kConvWarps);
+    }
+    for (int e = 0; e < 2 * S; ++e) mbar_init(&exp_full[e], kConvWarps);
+    for (int a = 0; a < kASlots; ++a) {
+      mbar_init(&a_full[a], kDeqWarps);
+      mbar_init(&a_empty[a], 1);
+    }
+    for (int d = 0; d < 2; ++d) {
+      mbar_init(&d_full[d], 1);
+      mbar_init(&d_empty[d], kAccWarps);
+    }
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == kWarpMma) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  fence_proxy_async_smem();            // the zeroed operand rows, for the MMA
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  // Let the next kernel in the stream launch now: its CTAs take the SM room
+  // this grid leaves free and prefetch their weights while this one runs.
+  // (They read this kernel's results only after griddepcontrol.wait, which
+  // waits for the whole grid to complete.)
+  if (threadIdx.x == 0) griddep_launch_dependents();
+
+  if (warp == kWarpProducer) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tensormap(&tm_w);
+      prefetch_tensormap(&tm_s);
+      prefetch_tensormap(&tm_x);
+      const uint64_t pol_stream = policy_evict_first();
+      const uint64_t pol_keep = policy_evict_last();
+      const uint32_t tx = static_cast<uint32_t>(kRows * (kStageK / 2 + kStageK / 16) +
+                                                M * kStageK * 2);
+      auto issue_weights = [&](int it, int slot) {
+        uint8_t* st = smem + slot * L.stage_bytes;
+        const int k0 = (st_begin + it) * kStageK;
+        tma_load_2d_hint(st, &tm_w, &full[slot], k0 / 2, row0, pol_stream);
+        tma_load_2d_hint(st + kHalfRows * 128, &tm_w, &full[slot], k0 / 2, row1, pol_stream);
+        tma_load_2d_hint(st + L.s_off, &tm_s, &full[slot], k0 / 16, row0, pol_stream);
+        tma_load_2d_hint(st + L.s_off + kHalfRows * 16, &tm_s, &full[slot], k0 / 16, row1,
+                         pol_stream);
+      };
+      auto issue_acts = [&](int it, int slot) {
+        uint8_t* st = smem + slot * L.stage_bytes;
+        tma_load_2d_hint(st + L.x_off, &tm_x, &full[slot], (st_begin + it) * kStageK, 0,
+                         pol_keep);
+      };
+      // The weights do not depend on the preceding kernel in the stream:
+      // fill the ring with them first, then wait for that kernel before
+      // touching the activations.
+      const int pre = n_stages < S ? n_stages : S;
+      for (int it = 0; it < pre; ++it) {
+        mbar_arrive_expect_tx(&full[it], tx);
+        issue_weights(it, it);
+      }
+      griddep_wait();
+      for (int it = 0; it < pre; ++it) issue_acts(it, it);
+      int issued = pre;
+      int slot = pre == S ? 0 : pre;
+      uint32_t par = pre == S ? 0u : 1u;
+      for (int it = pre; it < n_stages; ++it) {
+        if (!mbar_wait(&empty[slot], par, abort_flag)) break;
+        mbar_arrive_expect_tx(&full[slot], tx);
+        issue_weights(it, slot);
+        issue_acts(it, slot);
+        ++issued;
+        slot = next_slot(slot, S, par);
+      }
+      // Drain: never leave a copy in flight into this CTA's shared memory.
+      const int first = issued > S ? issued - S : 0;
+      for (int it = first; it < issued; ++it) {
+        volatile int no_abort = 0;
+        if (!mbar_wait(&full[it % S], (it / S) & 1, &no_abort)) atomicOr(p.err, kErrWaitTimeout);
+      }
+    }
+  } else if (warp == kWarpMma) {
+    // ------------------------------------------------------------ MMA issue
+    if (lane == 0) {
+      constexpr uint32_t idesc = umma_idesc_f16(kRows, NM);
+      int slot = 0, aslot = 0;
+      uint32_t par = 0, apar = 0;
+      int issued = 0;
+      for (int it = 0; it < n_stages; ++it) {
+        const int dbuf = it & 1;
+        if (!mbar_wait(&b_full[slot], par, abort_flag)) break;
+        if (!mbar_wait(&d_empty[dbuf], ((it >> 1) & 1) ^ 1u, abort_flag)) break;
+        const uint32_t b_base = smem_addr(smem + slot * L.stage_bytes + L.b_off);
+        const uint32_t d_tmem = tmem + kDCol + dbuf * NM;
+        bool ok = true;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          if (!mbar_wait(&a_full[aslot], apar, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            // 16 k per instruction: column block (2h + kk/4) of the operand,
+            // 32-byte step within its 128-byte swizzled rows.
+            const uint64_t b_desc =
+                umma_desc_sw128(b_base + (2 * h + kk / 4) * (NM * 128) + (kk % 4) * 32);
+            umma_f16_tmem_a(d_tmem, tmem + aslot * kAColsPerSlot + kk * 8, b_desc, idesc,
+                            (h | kk) != 0);
+          }
+          ++issued;
+          umma_commit(&a_empty[aslot]);
+          aslot = next_slot(aslot, kASlots, apar);
+        }
+        if (!ok) break;
+        umma_commit(&empty[slot]);
+        umma_commit(&d_full[dbuf]);
+        slot = next_slot(slot, S, par);
+      }
+      // Every MMA issued must have completed before TMEM is released.
+      umma_commit(mma_done);
+      volatile int no_abort = 0;
+      if (!mbar_wait(mma_done, 0, &no_abort)) atomicOr(p.err, kErrWaitTimeout);
+    }
+  } else if (warp < kWarpDeq) {
+    // ------------------------------------------------------------ converters
+    // Converter c takes activation rows c, c+2, ...; lane l the 16-byte
+    // chunk l (8 consecutive k) of each.  Row m of stage s is stored as
+    // f16(x * 2^a) with a = the largest exponent keeping the row's maximum
+    // |x| within this stage below 2^15.
+    const int c = warp - kWarpConv;
+    const int q = lane >> 3, c16 = lane & 7;       // 64-k column block, 16-B unit
+    int slot = 0, e = 0;
+    uint32_t par = 0, epar = 0;
+    for (int it = 0; it < n_stages; ++it) {
+      if (!warp_wait(&full[slot], par, abort_flag)) break;
+      uint8_t* st = smem + slot * L.stage_bytes;
+      for (int m = c; m < M; m += kConvWarps) {
+        const uint4 v = *reinterpret_cast<const uint4*>(st + L.x_off + m * 512 + lane * 16);
+        uint32_t mx = max_u16x2(max_u16x2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
+                                max_u16x2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
+        mx = __reduce_max_sync(0xffffffffu, max(mx & 0xFFFFu, mx >> 16));
+        const int e_max = static_cast<int>(mx >> 7);           // biased bf16 exponent
+        const int a = min(126, max(-126, 141 - e_max));        // max * 2^a < 2^15
+        const float f = pow2f(a);
+        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          o[j] = f32x2_to_f16x2(__uint_as_float(w4[j] << 16) * f,
+                                __uint_as_float(w4[j] & 0xFFFF0000u) * f);
+        *reinterpret_cast<uint4*>(st + L.b_off + q * (NM * 128) + (m >> 3) * 1024 +
+                                  (m & 7) * 128 + ((c16 ^ (m & 7)) << 4)) =
+            make_uint4(o[0], o[1], o[2], o[3]);
+        if (lane == 0) exps[e * kMaxRows + m] = a;
+      }
+      fence_proxy_async_smem();      // the operand, for the tensor core
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&b_full[slot]);
+        mbar_arrive(&exp_full[e]);
+      }
+      slot = next_slot(slot, S, par);
+      e = next_slot(e, 2 * S, epar);
+    }
+  } else if (warp < kWarpAcc) {
+    // ------------------------------------------------------------ dequantisers
+    // Warp (quadrant q, k half kh): lane = weight row 32q + lane = its TMEM
+    // lane; per half stage it writes k [64kh, 64kh + 64) of that row.
+    const int dw = warp - kWarpDeq;
+    const int q = warp & 3, kh = dw >> 2;
+    const int row = 32 * q + lane;
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(32 * q) << 16) + kh * 32;
+    int slot = 0, aslot = 0;
+    uint32_t par = 0, apar = 0;
+    bool ok = true;
+    for (int it = 0; it < n_stages && ok; ++it) {
+      if (!warp_wait(&full[slot], par, abort_flag)) break;
+      const uint8_t* st = smem + slot * L.stage_bytes;
+      const uint4 sc = *reinterpret_cast<const uint4*>(st + L.s_off + row * 16);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        if (!warp_wait(&a_empty[aslot], apar ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        // 64 k = two 16-byte code chunks of the row's 128-byte line
+        const int c0 = 4 * h + 2 * kh;
+        const uint4 w0 = *reinterpret_cast<const uint4*>(st + row * 128 + ((c0 ^ (row & 7)) << 4));
+        const uint4 w1 =
+            *reinterpret_cast<const uint4*>(st + row * 128 + (((c0 + 1) ^ (row & 7)) << 4));
+        // their four 16-k blocks' scales: bytes 8h + 4kh .. +3 of the row
+        const uint32_t s4 = h == 0 ? (kh ? sc.y : sc.x) : (kh ? sc.w : sc.z);
+        const uint32_t S0 = lut[s4 & 0xFFu], S1 = lut[(s4 >> 8) & 0xFFu];
+        const uint32_t S2 = lut[(s4 >> 16) & 0xFFu], S3 = lut[s4 >> 24];
+        uint32_t out[32];
+        dequant8_f16(w0.x, S0, &out[0]);
+        dequant8_f16(w0.y, S0, &out[4]);
+        dequant8_f16(w0.z, S1, &out[8]);
+        dequant8_f16(w0.w, S1, &out[12]);
+        dequant8_f16(w1.x, S2, &out[16]);
+        dequant8_f16(w1.y, S2, &out[20]);
+        dequant8_f16(w1.z, S3, &out[24]);
+        dequant8_f16(w1.w, S3, &out[28]);
+        tmem_st_32cols(t_lane + aslot * kAColsPerSlot, out);
+        tmem_st_wait();
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&a_full[aslot]);
+        aslot = next_slot(aslot, kASlots, apar);
+      }
+      slot = next_slot(slot, S, par);
+    }
+  }
+
+  // ---------------------------------------------------------------- accumulators
+  // Warp (quadrant q): lane = weight row 32q + lane; acc[m] sums
+  // D_stage[row][m] * 2^-a(stage, m) over this CTA's stages.
+  float acc[NM];
+#pragma unroll
+  for (int m = 0; m < NM; ++m) acc[m] = 0.f;
+  if (warp >= kWarpAcc) {
+    const int q = warp & 3;
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(32 * q) << 16) + kDCol;
+    int e = 0;
+    uint32_t epar = 0;
+    for (int it = 0; it < n_stages; ++it) {
+      const int dbuf = it & 1;
+      if (!warp_wait(&d_full[dbuf], (it >> 1) & 1, abort_flag)) break;
+      if (!warp_wait(&exp_full[e], epar, abort_flag)) break;
+      tc_fence_after_sync();
+      const int* ex = exps + e * kMaxRows;
+#pragma unroll
+      for (int half = 0; half < NM / 16; ++half) {
+        uint32_t d[16];
+        tmem_ld_16cols(t_lane + dbuf * NM + 16 * half, d);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int m = 16 * half + j;
+          if (m < M) acc[m] = fmaf(__uint_as_float(d[j]), pow2f(-ex[m]), acc[m]);
+        }
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&d_empty[dbuf]);
+      e = next_slot(e, 2 * S, epar);
+    }
+  }
+
+  if (*abort_flag && threadIdx.x == 0) atomicOr(p.err, kErrWaitTimeout);
+  // Every role is done with the ring and TMEM: release TMEM, then reuse the
+  // ring for the partial sums [128 rows][NM].
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == kWarpMma) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+  float* part = reinterpret_cast<float*>(smem);
+  if (warp >= kWarpAcc) {
+    const int row = 32 * (warp & 3) + lane;
+#pragma unroll
+    for (int m = 0; m < NM; ++m)
+      if (m < M) part[row * NM + m] = acc[m];
+  }
+
+  // ---------------------------------------------------------------- epilogue
+  // Every CTA of the cluster finishes its partial; CTA z then reduces a
+  // 1/split share of the outputs across the cluster's shared memories.
+  // (Reconverge each warp first: the cluster barrier is a warp-aligned op.)
+  __syncwarp();
+  if (split > 1)
+    cluster_sync();
+  else
+    __syncthreads();
+  {
+    const int R = p.swiglu ? kHalfRows : kRows;            // outputs per activation row
+    const int items = R * M;
+    const int i0 = static_cast<int>((int64_t)items * z / split);
+    const int i1 = static_cast<int>((int64_t)items * (z + 1) / split);
+    const uint32_t part_local = smem_addr(part);
+    const int64_t n_out = p.swiglu ? p.N / 2 : p.N;
+    const int64_t n_base = static_cast<int64_t>(blockIdx.x) * R;
+    for (int i = i0 + threadIdx.x; i < i1; i += kThreads) {
+      const int m = i / R, j = i % R;
+      float v = 0.f, u = 0.f;
+      if (split == 1) {
+        v = part[j * NM + m];
+        if (p.swiglu) u = part[(kHalfRows + j) * NM + m];
+      } else {
+        for (int c = 0; c < split; ++c) {
+          const uint32_t base = map_to_rank(part_local, c);
+          v += ld_cluster_f32(base + 4u * (j * NM + m));
+          if (p.swiglu) u += ld_cluster_f32(base + 4u * ((kHalfRows + j) * NM + m));
+        }
+      }
+      float yv = v * p.out_scale;
+      if (p.swiglu) yv = silu_mul(yv, u * p.out_scale);
+      const int64_t off = static_cast<int64_t>(m) * n_out + n_base + j;
+      if (p.out_f32)
+        static_cast<float*>(p.y)[off] = yv;
+      else
+        static_cast<__nv_bfloat16*>(p.y)[off] = __float2bfloat16_rn(yv);
+    }
+  }
+  if (split > 1) {
+    __syncwarp();
+    cluster_sync();   // keep every partial alive until all readers are done
+  }
+}
+
+}  // namespace gemvtc
+}  // namespace nvfp4

@@ -10,12 +10,14 @@
 #include <mutex>
 
 #include "../../include/nvfp4_linear.h"
+#include "gemv_tc.cuh"
 #include "smallm.cuh"
 #include "tcgemm.cuh"
 
 namespace {
 
 namespace sm = nvfp4::smallm;
+namespace gt = nvfp4::gemvtc;
 
 // Weight and scale bytes one 16-row group brings per 256-k stage, and the
 // weight bytes an SM should keep in flight (HBM latency x its bandwidth share).
@@ -62,6 +64,7 @@ struct DeviceInfo {
   int smem_per_sm = 0, smem_reserved = 0, regs_per_sm = 0, threads_per_sm = 0;
   unsigned int* err = nullptr;         // device address of g_device_error
   int smallm_regs[2][5][sm::kMaxGroups + 1] = {};  // registers per thread by (f16, MT, G)
+  int gemv_regs[2] = {};               // registers per thread of the tcgen05 few-row kernel (N 16, 32)
 };
 
 std::mutex g_mutex;
@@ -82,6 +85,20 @@ cudaError_t prepare_smallm(DeviceInfo& d) {
     if (e != cudaSuccess) return e;
     d.smallm_regs[F16 ? 1 : 0][MT][g] = fa.numRegs;
   }
+  return cudaSuccess;
+}
+
+template <int NM>
+cudaError_t prepare_gemv(DeviceInfo& d) {
+  const auto kern = &gt::gemv_tc_kernel<NM>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, d.max_smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  cudaFuncAttributes fa;
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, kern);
+  if (e != cudaSuccess) return e;
+  d.gemv_regs[NM == 16 ? 0 : 1] = fa.numRegs;
   return cudaSuccess;
 }
 
@@ -137,6 +154,7 @@ int device_setup(DeviceInfo** out) {
           prepare_smallm<3, false>(d) != cudaSuccess ||
           prepare_smallm<4, false>(d) != cudaSuccess ||
           prepare_smallm<1, true>(d) != cudaSuccess ||
+          prepare_gemv<16>(d) != cudaSuccess || prepare_gemv<32>(d) != cudaSuccess ||
           cudaFuncSetAttribute(nvfp4::tcgemm::tcgemm_kernel,
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                nvfp4::tcgemm::kSmemBytes) != cudaSuccess) {
@@ -221,14 +239,19 @@ int validate(const void* x, const void* wp, const void* ws, const void* y, int64
   if (!wp || !ws || (M > 0 && (!x || !y))) return NVFP4_ERR_INVALID;
   if (flags & ~(NVFP4_FLAG_SWIGLU | NVFP4_FLAG_F32_OUT | NVFP4_FLAG_FORCE_SMALLM |
                 NVFP4_FLAG_FORCE_TCGEMM | NVFP4_FLAG_SPLIT_MASK | NVFP4_FLAG_GROUPS_MASK |
-                NVFP4_FLAG_BF16_MMA))
+                NVFP4_FLAG_BF16_MMA | NVFP4_FLAG_FORCE_GEMV))
     return NVFP4_ERR_INVALID;
   if (((flags & NVFP4_FLAG_SPLIT_MASK) >> NVFP4_FLAG_SPLIT_SHIFT) > sm::kMaxSplit ||
       ((flags & NVFP4_FLAG_GROUPS_MASK) >> NVFP4_FLAG_GROUPS_SHIFT) > sm::kMaxGroups)
     return NVFP4_ERR_INVALID;
-  if ((flags & NVFP4_FLAG_FORCE_SMALLM) && (flags & NVFP4_FLAG_FORCE_TCGEMM))
+  const unsigned int force = flags & (NVFP4_FLAG_FORCE_SMALLM | NVFP4_FLAG_FORCE_TCGEMM |
+                                      NVFP4_FLAG_FORCE_GEMV);
+  if (force & (force - 1)) return NVFP4_ERR_INVALID;        // at most one
+  if ((flags & NVFP4_FLAG_BF16_MMA) && (flags & (NVFP4_FLAG_FORCE_TCGEMM | NVFP4_FLAG_FORCE_GEMV)))
     return NVFP4_ERR_INVALID;
-  if ((flags & NVFP4_FLAG_FORCE_SMALLM) && M > kSmallMMax) return NVFP4_ERR_INVALID;
+  if ((flags & (NVFP4_FLAG_FORCE_SMALLM | NVFP4_FLAG_FORCE_GEMV | NVFP4_FLAG_BF16_MMA)) &&
+      M > kSmallMMax)
+    return NVFP4_ERR_INVALID;
   const uintptr_t mis = reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(wp) |
                         reinterpret_cast<uintptr_t>(ws) | reinterpret_cast<uintptr_t>(y);
   if (mis & 15u) return NVFP4_ERR_MISALIGNED;
@@ -239,10 +262,17 @@ int validate(const void* x, const void* wp, const void* ws, const void* y, int64
   return NVFP4_OK;
 }
 
+// Kernel by M, from measurements on GB300 (graph-timed, the 5120 x 34816
+// projection): M <= 8 the warp-MMA kernel (f16) is fastest; M = 9..16 the
+// tcgen05 few-row kernel (2 CTAs per SM); M = 17..32 the warp-MMA kernel
+// again, where the tcgen05 one runs a single CTA per SM and its lone MMA
+// issuer (about 60 ns per tcgen05.mma whatever N is) bounds it.
 int kernel_for(int64_t M, unsigned int flags) {
-  if (flags & NVFP4_FLAG_FORCE_SMALLM) return NVFP4_KERNEL_SMALLM;
+  if (flags & (NVFP4_FLAG_FORCE_SMALLM | NVFP4_FLAG_BF16_MMA)) return NVFP4_KERNEL_SMALLM;
   if (flags & NVFP4_FLAG_FORCE_TCGEMM) return NVFP4_KERNEL_TCGEMM;
-  return M <= kSmallMMax ? NVFP4_KERNEL_SMALLM : NVFP4_KERNEL_TCGEMM;
+  if (flags & NVFP4_FLAG_FORCE_GEMV) return NVFP4_KERNEL_GEMV;
+  if (M > kSmallMMax) return NVFP4_KERNEL_TCGEMM;
+  return (M > 8 && M <= 16) ? NVFP4_KERNEL_GEMV : NVFP4_KERNEL_SMALLM;
 }
 
 struct SmallmPlan {
@@ -374,6 +404,111 @@ int launch_smallm(const DeviceInfo& d, const void* x, const uint8_t* wp, const u
   return NVFP4_OK;
 }
 
+struct GemvPlan {
+  int split = 0;
+  int stages = 0;
+  int64_t row_blocks = 0;
+};
+
+// The tcgen05 few-row kernel: 128 weight rows per CTA.  Ring depth: the
+// deepest that keeps the most CTAs resident per SM.  Split: the cost is the
+// busiest SM's stages (ceil(CTAs / SMs) x (stages per CTA + a fixed
+// per-CTA cost)); grids resident in one wave win over those that are not;
+// ties go to fewer CTAs.  NVFP4_FLAG_SPLIT pins the split.
+template <int NM>
+GemvPlan plan_gemv(const DeviceInfo& d, int64_t M, int64_t N, int64_t K, unsigned int flags) {
+  GemvPlan best;
+  const int64_t T = K / gt::kStageK;
+  const int want_split = (flags & NVFP4_FLAG_SPLIT_MASK) >> NVFP4_FLAG_SPLIT_SHIFT;
+  const int regs = d.gemv_regs[NM == 16 ? 0 : 1];
+  int occ = 0, stages = 0;
+  for (int s = 2; s <= 8; ++s) {
+    const gt::SmemLayout lay = gt::make_layout(NM, static_cast<int>(M), s);
+    if (lay.total > d.max_smem || !gt::layout_ok(lay, NM)) continue;
+    const int o = resident_ctas(d, gt::kThreads, regs, lay.total);
+    if (o > occ || (o == occ && o > 0)) {
+      occ = o;
+      stages = s;
+    }
+  }
+  if (occ == 0) return best;
+  best.stages = stages;
+  best.row_blocks = N / gt::kRows;                  // SwiGLU: 64 gate + 64 up rows, same count
+  const int64_t slots = static_cast<int64_t>(d.num_sms) * occ;
+  double best_cost = -1.0;
+  int64_t best_ctas = 0;
+  bool best_one_wave = false;
+  const int s_max = static_cast<int>(std::min<int64_t>(T, gt::kMaxSplit));
+  for (int s = 1; s <= s_max; ++s) {
+    if (want_split && s != want_split) continue;
+    const int64_t ctas = best.row_blocks * s;
+    const bool one_wave = ctas <= slots;
+    const int64_t per_sm = (ctas + d.num_sms - 1) / d.num_sms;
+    const double cost = static_cast<double>(per_sm) * (static_cast<double>((T + s - 1) / s) + 1.5);
+    const bool better =
+        best_cost < 0 || (one_wave && !best_one_wave) ||
+        (one_wave == best_one_wave &&
+         (cost < best_cost * 0.999 || (cost <= best_cost * 1.001 && ctas < best_ctas)));
+    if (better) {
+      best_cost = cost;
+      best_ctas = ctas;
+      best_one_wave = one_wave;
+      best.split = s;
+    }
+  }
+  if (best.split == 0) best.stages = 0;
+  return best;
+}
+
+template <int NM>
+int launch_gemv(const DeviceInfo& d, const void* x, const uint8_t* wp, const uint8_t* ws,
+                float gs, void* y, int64_t M, int64_t N, int64_t K, unsigned int flags,
+                cudaStream_t stream) {
+  const GemvPlan plan = plan_gemv<NM>(d, M, N, K, flags);
+  if (plan.stages == 0) return NVFP4_ERR_INVALID;   // an override that cannot run
+  CUtensorMap tw, ts, tx;
+  if (!encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, wp, K / 2, N, K / 2, 128, gt::kHalfRows,
+                 CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT8, ws, K / 16, N, K / 16, 16, gt::kHalfRows,
+                 CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !encode_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, K, M, K * 2, gt::kStageK,
+                 static_cast<uint32_t>(M), CU_TENSOR_MAP_SWIZZLE_NONE))
+    return NVFP4_ERR_LAUNCH;
+  gt::Params p;
+  p.y = y;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.out_scale = static_cast<float>(1.0 / static_cast<double>(gs));   // f16 weights are exact
+  p.stages_total = static_cast<int>(K / gt::kStageK);
+  p.split = plan.split;
+  p.lay = gt::make_layout(NM, static_cast<int>(M), plan.stages);
+  p.out_f32 = (flags & NVFP4_FLAG_F32_OUT) ? 1 : 0;
+  p.swiglu = (flags & NVFP4_FLAG_SWIGLU) ? 1 : 0;
+  p.err = d.err;
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof cfg);
+  cfg.gridDim = dim3(static_cast<unsigned>(plan.row_blocks), static_cast<unsigned>(plan.split), 1);
+  cfg.blockDim = dim3(gt::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = p.lay.total;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = static_cast<unsigned>(plan.split);
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, gt::gemv_tc_kernel<NM>, tw, ts, tx, p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return NVFP4_ERR_LAUNCH;
+  }
+  return NVFP4_OK;
+}
+
 int launch_tcgemm(const DeviceInfo& d, const void* x, const uint8_t* wp, const uint8_t* ws,
                   float gs, void* y, int64_t M, int64_t N, int64_t K, unsigned int flags,
                   cudaStream_t stream) {
@@ -425,7 +560,12 @@ int run(const void* x, const uint8_t* wp, const uint8_t* ws, float gs, void* y, 
   st = device_setup(&d);
   if (st != NVFP4_OK) return st;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
-  if (kernel_for(M, flags) == NVFP4_KERNEL_SMALLM) {
+  const int kernel = kernel_for(M, flags);
+  if (kernel == NVFP4_KERNEL_GEMV) {
+    if (M <= 16) return launch_gemv<16>(*d, x, wp, ws, gs, y, M, N, K, flags, stream);
+    return launch_gemv<32>(*d, x, wp, ws, gs, y, M, N, K, flags, stream);
+  }
+  if (kernel == NVFP4_KERNEL_SMALLM) {
     switch ((M + 7) / 8) {
       case 1:
         if (!(flags & NVFP4_FLAG_BF16_MMA))

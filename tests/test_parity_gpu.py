@@ -56,25 +56,47 @@ def full_check(t, flags=0, what=""):
 
 
 # ------------------------------------------------------------------ small M
+# The two few-row kernels, each forced (the default picks one by M).
+FEW_ROW = [pytest.param(_lib.FLAG_FORCE_GEMV, id="gemv_tc"),
+           pytest.param(_lib.FLAG_FORCE_SMALLM, id="smallm")]
+
+
+@pytest.mark.parametrize("kflag", FEW_ROW)
 @pytest.mark.parametrize("M", [1, 2, 5, 7, 8, 9, 16, 17, 24, 25, 31, 32])
-def test_smallm_all_row_counts(M):
+def test_few_row_all_row_counts(M, kflag):
     t = make_linear(M, 384, 1024, seed=100 + M)
-    assert _lib.kernel_for(M, 384, 1024) == _lib.KERNEL_SMALLM
-    full_check(t, what="smallm M=%d" % M)
+    want = _lib.KERNEL_SMALLM if kflag == _lib.FLAG_FORCE_SMALLM else _lib.KERNEL_GEMV
+    assert _lib.kernel_for(M, 384, 1024, kflag) == want
+    assert _lib.kernel_for(M, 384, 1024) in (_lib.KERNEL_SMALLM, _lib.KERNEL_GEMV)
+    full_check(t, kflag, what="few-row M=%d flags=%d" % (M, kflag))
 
 
+@pytest.mark.parametrize("kflag", FEW_ROW)
 @pytest.mark.parametrize("N,K", [(128, 256), (256, 768), (640, 4352), (1024, 2304)])
-def test_smallm_shapes_and_uneven_splits(N, K):
-    # K/256 stages split over clusters of up to 8 CTAs, unevenly when they
-    # do not divide
+def test_few_row_shapes_and_uneven_splits(N, K, kflag):
+    # K/256 stages split over clusters of CTAs, unevenly when they do not
+    # divide
     t = make_linear(7, N, K, seed=N + K)
-    full_check(t, what="smallm N=%d K=%d" % (N, K))
+    full_check(t, kflag, what="few-row N=%d K=%d flags=%d" % (N, K, kflag))
 
 
-@pytest.mark.parametrize("M", [1, 7, 32])
-def test_smallm_swiglu(M):
+@pytest.mark.parametrize("kflag", FEW_ROW)
+@pytest.mark.parametrize("M", [1, 7, 16, 17, 32])
+def test_few_row_swiglu(M, kflag):
     t = make_linear(M, 512, 1024, seed=300 + M)
-    full_check(t, _lib.FLAG_SWIGLU, what="smallm swiglu M=%d" % M)
+    full_check(t, _lib.FLAG_SWIGLU | kflag, what="few-row swiglu M=%d flags=%d" % (M, kflag))
+
+
+@pytest.mark.parametrize("M", [1, 7, 16, 32])
+def test_gemv_tc_every_split(M):
+    """The tcgen05 few-row kernel at every k split (one cluster of s CTAs,
+    uneven when s does not divide the K/256 stages), forced."""
+    N, K = 640, 4096
+    t = make_linear(M, N, K, seed=1050 + M)
+    y64, a = _oracle(t)
+    for s in (1, 2, 3, 5, 7, 8, 16):
+        _check_against(t, y64, a, _lib.FLAG_FORCE_GEMV | _lib.FLAG_SPLIT(s),
+                       "gemv_tc M=%d split=%d" % (M, s))
 
 
 # ------------------------------------------------------------------ tcgen05
@@ -98,10 +120,11 @@ def test_tcgemm_swiglu(M):
 
 
 @pytest.mark.parametrize("M", [1, 7, 32])
-def test_both_kernels_agree_at_small_m(M):
+def test_every_kernel_at_small_m(M):
     t = make_linear(M, 256, 512, seed=500 + M)
     full_check(t, _lib.FLAG_FORCE_TCGEMM, what="forced tcgemm M=%d" % M)
     full_check(t, _lib.FLAG_FORCE_SMALLM, what="forced smallm M=%d" % M)
+    full_check(t, _lib.FLAG_FORCE_GEMV, what="forced gemv_tc M=%d" % M)
 
 
 def _oracle(t):
@@ -120,7 +143,7 @@ def _check_against(t, y64, a, flags, what):
 def test_smallm_every_cta_height_and_split(M):
     """Every CTA height (16*g rows, g = 1..8; ragged row tails where 16*g
     does not divide N) and k split (one cluster of s CTAs, uneven when s
-    does not divide the K/256 stages) the planner may pick, forced."""
+    does not divide the K/256 stages) of the warp-MMA kernel, forced."""
     N, K = 640, 4096
     t = make_linear(M, N, K, seed=1000 + M)
     y64, a = _oracle(t)
@@ -128,7 +151,7 @@ def test_smallm_every_cta_height_and_split(M):
     ran = 0
     for g in range(1, g_max + 1):
         for s in (1, 2, 3, 5, 8, 16):
-            flags = _lib.FLAG_GROUPS(g) | _lib.FLAG_SPLIT(s)
+            flags = _lib.FLAG_FORCE_SMALLM | _lib.FLAG_GROUPS(g) | _lib.FLAG_SPLIT(s)
             try:
                 _check_against(t, y64, a, flags, "M=%d g=%d split=%d" % (M, g, s))
                 ran += 1
@@ -141,17 +164,21 @@ def test_smallm_every_cta_height_and_split(M):
 def test_smallm_swiglu_overrides(M):
     t = make_linear(M, 1024, 2048, seed=1100 + M)
     for g, s in ((1, 1), (2, 3), (4, 8)):
-        full_check(t, _lib.FLAG_SWIGLU | _lib.FLAG_GROUPS(g) | _lib.FLAG_SPLIT(s),
-                   what="swiglu M=%d g=%d split=%d" % (M, g, s))
+        full_check(t, _lib.FLAG_SWIGLU | _lib.FLAG_FORCE_SMALLM | _lib.FLAG_GROUPS(g) |
+                   _lib.FLAG_SPLIT(s), what="swiglu M=%d g=%d split=%d" % (M, g, s))
+    for s in (1, 3, 8):
+        full_check(t, _lib.FLAG_SWIGLU | _lib.FLAG_FORCE_GEMV | _lib.FLAG_SPLIT(s),
+                   what="gemv_tc swiglu M=%d split=%d" % (M, s))
 
 
-@pytest.mark.parametrize("M", [1, 3, 8])
+@pytest.mark.parametrize("M", [1, 3, 8, 20])
 def test_smallm_bf16_multiply_path(M):
-    """M <= 8 defaults to f16 operands; the bf16 path is kept as an option
-    and must meet the same bound."""
+    """The few-row kernels default to f16 operands; the warp-MMA kernel's
+    bf16 path is kept as an option and must meet the same bound."""
     t = make_linear(M, 384, 2048, seed=1200 + M)
     full_check(t, _lib.FLAG_BF16_MMA, what="bf16-mma M=%d" % M)
     full_check(t, 0, what="f16 M=%d" % M)
+    full_check(t, _lib.FLAG_FORCE_GEMV, what="gemv_tc M=%d" % M)
 
 
 def _wide_range_inputs(M, seed):
@@ -180,9 +207,15 @@ def _wide_range_inputs(M, seed):
     return LinearInputs(f32_to_bf16_bits(x), wp, ws, GLOBAL_SCALE)
 
 
-@pytest.mark.parametrize("M,flags", [(4, 0), (8, 0), (4, _lib.FLAG_BF16_MMA), (12, 0),
-                                     (40, 0), (4, _lib.FLAG_SPLIT(1)), (4, _lib.FLAG_SPLIT(8)),
-                                     (8, _lib.FLAG_SPLIT(3))])
+@pytest.mark.parametrize("M,flags", [(4, 0), (8, 0), (12, 0), (32, 0), (4, _lib.FLAG_BF16_MMA),
+                                     (40, 0), (4, _lib.FLAG_FORCE_GEMV | _lib.FLAG_SPLIT(1)),
+                                     (4, _lib.FLAG_FORCE_GEMV | _lib.FLAG_SPLIT(8)),
+                                     (8, _lib.FLAG_FORCE_GEMV | _lib.FLAG_SPLIT(3)),
+                                     (32, _lib.FLAG_FORCE_GEMV),
+                                     (4, _lib.FLAG_FORCE_SMALLM),
+                                     (4, _lib.FLAG_FORCE_SMALLM | _lib.FLAG_SPLIT(8)),
+                                     (8, _lib.FLAG_FORCE_SMALLM | _lib.FLAG_SPLIT(3)),
+                                     (12, _lib.FLAG_FORCE_SMALLM)])
 def test_wide_dynamic_range_rows(M, flags):
     t = _wide_range_inputs(M, seed=1300 + M)
     y64, a = _oracle(t)
@@ -196,6 +229,8 @@ def test_wide_dynamic_range_rows(M, flags):
 
 
 @pytest.mark.parametrize("M,flags", [(1, 0), (6, 0), (6, _lib.FLAG_BF16_MMA), (20, 0),
+                                     (1, _lib.FLAG_FORCE_SMALLM), (6, _lib.FLAG_FORCE_SMALLM),
+                                     (1, _lib.FLAG_FORCE_GEMV), (6, _lib.FLAG_FORCE_GEMV),
                                      (6, _lib.FLAG_FORCE_TCGEMM), (50, 0)])
 def test_non_finite_values_propagate(M, flags):
     """An inf or NaN activation, or a NaN block scale (e4m3 S.1111.111),
@@ -241,7 +276,8 @@ def _exhaustive_products():
     return LinearInputs(x, wp, ws, np.float32(1.0))
 
 
-@pytest.mark.parametrize("flags", [_lib.FLAG_FORCE_SMALLM, _lib.FLAG_FORCE_TCGEMM])
+@pytest.mark.parametrize("flags", [_lib.FLAG_FORCE_SMALLM, _lib.FLAG_FORCE_TCGEMM,
+                                   _lib.FLAG_FORCE_GEMV])
 def test_every_code_times_every_scale_is_exact(flags):
     t = _exhaustive_products()
     y64, _ = oracle.linear_f64(t.x_bits, t.w_packed, t.w_scale, t.global_scale)
@@ -251,7 +287,8 @@ def test_every_code_times_every_scale_is_exact(flags):
     assert np.array_equal(y32[~nan], y64[~nan])
 
 
-@pytest.mark.parametrize("M,flags", [(5, 0), (70, 0), (5, _lib.FLAG_FORCE_TCGEMM)])
+@pytest.mark.parametrize("M,flags", [(5, 0), (12, 0), (30, 0), (70, 0),
+                                     (5, _lib.FLAG_FORCE_TCGEMM), (5, _lib.FLAG_FORCE_GEMV)])
 def test_exact_integer_inputs_are_bit_exact(M, flags):
     # small-integer activations, power-of-two scales, global scale 1: every
     # partial sum is an exactly representable fp32 number, so the result is
@@ -268,17 +305,17 @@ def test_exact_integer_inputs_are_bit_exact(M, flags):
     assert np.array_equal(y32, y64)
 
 
-@pytest.mark.parametrize("M", [3, 50])
-def test_sign_flip_negates_exactly(M):
+@pytest.mark.parametrize("M,flags", [(3, 0), (3, _lib.FLAG_FORCE_GEMV), (50, 0)])
+def test_sign_flip_negates_exactly(M, flags):
     t = make_linear(M, 256, 512, seed=600 + M)
-    y = run(t, _lib.FLAG_F32_OUT).cpu().numpy()
+    y = run(t, _lib.FLAG_F32_OUT | flags).cpu().numpy()
     flipped = LinearInputs(t.x_bits, t.w_packed ^ np.uint8(0x88), t.w_scale, t.global_scale)
-    y_neg = run(flipped, _lib.FLAG_F32_OUT).cpu().numpy()
+    y_neg = run(flipped, _lib.FLAG_F32_OUT | flags).cpu().numpy()
     assert np.array_equal(y_neg, -y)
 
 
-@pytest.mark.parametrize("M", [1, 40])
-def test_nibble_order(M):
+@pytest.mark.parametrize("M,flags", [(1, 0), (1, _lib.FLAG_FORCE_GEMV), (40, 0)])
+def test_nibble_order(M, flags):
     K, N = 256, 128
     x = np.zeros((M, K), np.uint16)
     x[:, 0] = 0x3F80          # 1.0 at k = 0
@@ -288,19 +325,22 @@ def test_nibble_order(M):
     lo[:, 0] = 0x07           # 6.0 at k = 0 (low nibble)
     hi = np.zeros((N, K // 2), np.uint8)
     hi[:, 0] = 0x70           # 6.0 at k = 1 (high nibble)
-    y_lo = run(LinearInputs(x, lo, ws, np.float32(1.0)), _lib.FLAG_F32_OUT).cpu().numpy()
-    y_hi = run(LinearInputs(x, hi, ws, np.float32(1.0)), _lib.FLAG_F32_OUT).cpu().numpy()
+    y_lo = run(LinearInputs(x, lo, ws, np.float32(1.0)), _lib.FLAG_F32_OUT | flags).cpu().numpy()
+    y_hi = run(LinearInputs(x, hi, ws, np.float32(1.0)), _lib.FLAG_F32_OUT | flags).cpu().numpy()
     assert np.all(y_lo == 6.0) and np.all(y_hi == 12.0)
 
 
-def test_row_batch_invariance_verify_vs_decode():
+@pytest.mark.parametrize("kflag", FEW_ROW)
+def test_row_batch_invariance_verify_vs_decode(kflag):
     # greedy decode (M = 1) and speculative verify (M = 7) see the same rows:
     # each verify row must equal the single-row call on that row, bit for bit
+    # (same k split forced on both)
     t = make_linear(7, 1024, 2048, seed=700)
-    y7 = bf16_bits(run(t))
+    fl = kflag | _lib.FLAG_SPLIT(4)
+    y7 = bf16_bits(run(t, fl))
     for i in range(7):
         ti = LinearInputs(t.x_bits[i:i + 1].copy(), t.w_packed, t.w_scale, t.global_scale)
-        assert np.array_equal(bf16_bits(run(ti))[0], y7[i]), "row %d" % i
+        assert np.array_equal(bf16_bits(run(ti, fl))[0], y7[i]), "row %d" % i
 
 
 # ------------------------------------------------------------------ edges
@@ -329,7 +369,7 @@ def test_errors_on_device_buffers():
     assert st == -3
 
 
-@pytest.mark.parametrize("M", [3, 45])
+@pytest.mark.parametrize("M", [3, 20, 45])
 def test_output_guard_rows_untouched(M):
     t = make_linear(M, 256, 512, seed=800 + M)
     x, wp, ws = to_dev(t)
