@@ -50,19 +50,29 @@ constexpr int kStageK = 256;            // k per pipeline stage
 constexpr int kASlots = 3;              // TMEM weight ring, 128 k (64 columns) each
 constexpr int kAColsPerSlot = 64;
 constexpr int kDCol = kASlots * kAColsPerSlot;   // D buffers start at column 192
-constexpr uint32_t kTmemCols = 256;
 constexpr int kMaxRows = 32;            // activation rows served
 constexpr int kMaxSplit = 16;           // cluster size limit (non-portable above 8)
 
-constexpr int kWarpProducer = 0;
-constexpr int kWarpMma = 1;
-constexpr int kWarpConv = 2;            // two converter warps: 2, 3
-constexpr int kConvWarps = 2;
-constexpr int kWarpDeq = 4;             // eight dequantisation warps: 4..11
-constexpr int kDeqWarps = 8;
-constexpr int kWarpAcc = 12;            // four accumulator warps: 12..15
-constexpr int kAccWarps = 4;
-constexpr int kThreads = (kWarpAcc + kAccWarps) * 32;   // 512
+// Warp roles.  Two MMA issuers: a single thread issues at most one
+// tcgen05.mma every ~30-60 ns whatever the MMA's N, far below what the
+// tensor core accepts from several issuers, so half stage h of every stage
+// is issued by warp kWarpMma + h into its own accumulator.  N = 32 (up to
+// 32 activation rows) runs one CTA per SM and gets three converter warps.
+template <int NM>
+struct Roles {
+  static constexpr int kWarpProducer = 0;
+  static constexpr int kWarpMma = 1;                       // issuers: warps 1, 2
+  static constexpr int kWarpConv = 3;
+  static constexpr int kConvWarps = NM == 16 ? 1 : 3;
+  static constexpr int kWarpDeq = kWarpConv + kConvWarps;  // eight dequantisation warps
+  static constexpr int kDeqWarps = 8;
+  static constexpr int kWarpAcc = kWarpDeq + kDeqWarps;   // four accumulator warps
+  static constexpr int kAccWarps = 4;
+  static constexpr int kThreads = (kWarpAcc + kAccWarps) * 32;
+  // weight ring (192 columns) + accumulators [2 buffers][2 half stages][NM]
+  static constexpr uint32_t kTmemCols = NM == 16 ? 256 : 512;
+  static_assert(kDCol + 4 * NM <= static_cast<int>(kTmemCols), "TMEM plan");
+};
 
 __host__ __device__ constexpr int align_up(int v, int a) { return (v + a - 1) / a * a; }
 
@@ -83,7 +93,7 @@ struct SmemLayout {
   int total;        // dynamic shared memory to request (with alignment slack)
 };
 
-__host__ __device__ constexpr int num_barriers(int stages) { return 5 * stages + 11; }
+__host__ __device__ constexpr int num_barriers(int stages) { return 5 * stages + 12; }
 
 __host__ __device__ constexpr SmemLayout make_layout(int n_mma, int m_rows, int stages) {
   SmemLayout l{};
@@ -134,11 +144,13 @@ __device__ __forceinline__ int next_slot(int slot, int n, uint32_t& parity) {
 }
 
 template <int NM>
-__global__ void __launch_bounds__(kThreads, NM == 16 ? 2 : 1)
+__global__ void __launch_bounds__(Roles<NM>::kThreads, NM == 16 ? 2 : 1)
     gemv_tc_kernel(const __grid_constant__ CUtensorMap tm_w,
                    const __grid_constant__ CUtensorMap tm_s,
                    const __grid_constant__ CUtensorMap tm_x, const Params p) {
   static_assert(NM == 16 || NM == 32, "MMA N is 16 or 32");
+  using R = Roles<NM>;
+  constexpr int kThreads = R::kThreads;
   const SmemLayout& L = p.lay;
   const int S = L.stages;
   extern __shared__ uint8_t smem_raw[];
@@ -147,16 +159,16 @@ __global__ void __launch_bounds__(kThreads, NM == 16 ? 2 : 1)
   uint32_t* lut = reinterpret_cast<uint32_t*>(smem + L.lut_off);
   int* exps = reinterpret_cast<int*>(smem + L.exp_off);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bar_off);   // TMA landed
-  uint64_t* empty = full + S;          // stage consumed (MMA commit)
+  uint64_t* empty = full + S;          // stage consumed (both issuers' commits)
   uint64_t* b_full = empty + S;        // f16 activations written (converters)
   uint64_t* exp_full = b_full + S;     // [2S] exponents written (converters)
   uint64_t* a_full = exp_full + 2 * S; // [3] TMEM weights written (dequantisers)
   uint64_t* a_empty = a_full + kASlots;    // [3] TMEM weights consumed (MMA commit)
-  uint64_t* d_full = a_empty + kASlots;    // [2] stage accumulator ready (MMA commit)
-  uint64_t* d_empty = d_full + 2;          // [2] stage accumulator read (acc warps)
-  uint64_t* mma_done = d_empty + 2;        // every MMA issued has completed
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(mma_done + 1);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1) + 1;
+  uint64_t* d_full = a_empty + kASlots;    // [2] stage accumulators ready (both issuers)
+  uint64_t* d_empty = d_full + 2;          // [2] stage accumulators read (acc warps)
+  uint64_t* mma_done = d_empty + 2;        // [2] every MMA of issuer h has completed
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(mma_done + 2);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 2) + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int M = static_cast<int>(p.M);
@@ -187,24 +199,24 @@ __global__ void __launch_bounds__(kThreads, NM == 16 ? 2 : 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
-      mbar_init(&b_full[s], kConvWarps);
+      mbar_init(&empty[s], 2);
+      mbar_init(&b_full[s], R::kConvWarps);
     }
-    for (int e = 0; e < 2 * S; ++e) mbar_init(&exp_full[e], kConvWarps);
+    for (int e = 0; e < 2 * S; ++e) mbar_init(&exp_full[e], R::kConvWarps);
     for (int a = 0; a < kASlots; ++a) {
-      mbar_init(&a_full[a], kDeqWarps);
+      mbar_init(&a_full[a], R::kDeqWarps);
       mbar_init(&a_empty[a], 1);
     }
     for (int d = 0; d < 2; ++d) {
-      mbar_init(&d_full[d], 1);
-      mbar_init(&d_empty[d], kAccWarps);
+      mbar_init(&d_full[d], 2);
+      mbar_init(&d_empty[d], R::kAccWarps);
+      mbar_init(&mma_done[d], 1);
     }
-    mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == kWarpMma) {
-    tmem_alloc(tmem_slot, kTmemCols);
+  if (warp == R::kWarpMma) {
+    tmem_alloc(tmem_slot, R::kTmemCols);
     tmem_relinquish();
   }
   fence_proxy_async_smem();            // the zeroed operand rows, for the MMA
@@ -218,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, NM == 16 ? 2 : 1)
   // waits for the whole grid to complete.)
   if (threadIdx.x == 0) griddep_launch_dependents();
 
-  if (warp == kWarpProducer) {
+  if (warp == R::kWarpProducer) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       prefetch_tensormap(&tm_w);
@@ -270,64 +282,60 @@ __global__ void __launch_bounds__(kThreads, NM == 16 ? 2 : 1)
         if (!mbar_wait(&full[it % S], (it / S) & 1, &no_abort)) atomicOr(p.err, kErrWaitTimeout);
       }
     }
-  } else if (warp == kWarpMma) {
+  } else if (warp == R::kWarpMma || warp == R::kWarpMma + 1) {
     // ------------------------------------------------------------ MMA issue
+    // Issuer h takes half stage h (k [128h, 128h + 128)) of every stage:
+    // 8 MMAs of K = 16 into accumulator [dbuf][h].
     if (lane == 0) {
       constexpr uint32_t idesc = umma_idesc_f16(kRows, NM);
-      int slot = 0, aslot = 0;
-      uint32_t par = 0, apar = 0;
-      int issued = 0;
-      for (int it = 0; it < n_stages; ++it) {
+      const int h = warp - R::kWarpMma;
+      int slot = 0;
+      uint32_t par = 0;
+      int g = h;                                     // half-stage index 2 * it + h
+      for (int it = 0; it < n_stages; ++it, g += 2) {
         const int dbuf = it & 1;
+        const int aslot = g % kASlots;
+        const uint32_t apar = static_cast<uint32_t>(g / kASlots) & 1u;
         if (!mbar_wait(&b_full[slot], par, abort_flag)) break;
         if (!mbar_wait(&d_empty[dbuf], ((it >> 1) & 1) ^ 1u, abort_flag)) break;
-        const uint32_t b_base = smem_addr(smem + slot * L.stage_bytes + L.b_off);
-        const uint32_t d_tmem = tmem + kDCol + dbuf * NM;
-        bool ok = true;
+        if (!mbar_wait(&a_full[aslot], apar, abort_flag)) break;
+        tc_fence_after_sync();
+        // Operand column blocks 2h and 2h + 1; 32-byte steps within their
+        // 128-byte swizzled rows (the descriptor's address field counts 16 B).
+        const uint64_t b_desc0 =
+            umma_desc_sw128(smem_addr(smem + slot * L.stage_bytes + L.b_off) + 2 * h * (NM * 128));
+        const uint32_t d_tmem = tmem + kDCol + (2 * dbuf + h) * NM;
+        const uint32_t a_tmem = tmem + aslot * kAColsPerSlot;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          if (!mbar_wait(&a_full[aslot], apar, abort_flag)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after_sync();
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            // 16 k per instruction: column block (2h + kk/4) of the operand,
-            // 32-byte step within its 128-byte swizzled rows.
-            const uint64_t b_desc =
-                umma_desc_sw128(b_base + (2 * h + kk / 4) * (NM * 128) + (kk % 4) * 32);
-            umma_f16_tmem_a(d_tmem, tmem + aslot * kAColsPerSlot + kk * 8, b_desc, idesc,
-                            (h | kk) != 0);
-          }
-          ++issued;
-          umma_commit(&a_empty[aslot]);
-          aslot = next_slot(aslot, kASlots, apar);
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t b_desc =
+              b_desc0 + static_cast<uint64_t>(((kk / 4) * (NM * 128) + (kk % 4) * 32) >> 4);
+          umma_f16_tmem_a(d_tmem, a_tmem + kk * 8, b_desc, idesc, kk != 0);
         }
-        if (!ok) break;
+        umma_commit(&a_empty[aslot]);
         umma_commit(&empty[slot]);
         umma_commit(&d_full[dbuf]);
         slot = next_slot(slot, S, par);
       }
       // Every MMA issued must have completed before TMEM is released.
-      umma_commit(mma_done);
+      umma_commit(&mma_done[h]);
       volatile int no_abort = 0;
-      if (!mbar_wait(mma_done, 0, &no_abort)) atomicOr(p.err, kErrWaitTimeout);
+      if (!mbar_wait(&mma_done[h], 0, &no_abort)) atomicOr(p.err, kErrWaitTimeout);
     }
-  } else if (warp < kWarpDeq) {
+  } else if (warp < R::kWarpDeq) {
     // ------------------------------------------------------------ converters
     // Converter c takes activation rows c, c+2, ...; lane l the 16-byte
     // chunk l (8 consecutive k) of each.  Row m of stage s is stored as
     // f16(x * 2^a) with a = the largest exponent keeping the row's maximum
     // |x| within this stage below 2^15.
-    const int c = warp - kWarpConv;
+    const int c = warp - R::kWarpConv;
     const int q = lane >> 3, c16 = lane & 7;       // 64-k column block, 16-B unit
     int slot = 0, e = 0;
     uint32_t par = 0, epar = 0;
     for (int it = 0; it < n_stages; ++it) {
       if (!warp_wait(&full[slot], par, abort_flag)) break;
       uint8_t* st = smem + slot * L.stage_bytes;
-      for (int m = c; m < M; m += kConvWarps) {
+      for (int m = c; m < M; m += R::kConvWarps) {
         const uint4 v = *reinterpret_cast<const uint4*>(st + L.x_off + m * 512 + lane * 16);
         uint32_t mx = max_u16x2(max_u16x2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
                                 max_u16x2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
@@ -355,11 +363,11 @@ __global__ void __launch_bounds__(kThreads, NM == 16 ? 2 : 1)
       slot = next_slot(slot, S, par);
       e = next_slot(e, 2 * S, epar);
     }
-  } else if (warp < kWarpAcc) {
+  } else if (warp < R::kWarpAcc) {
     // ------------------------------------------------------------ dequantisers
     // Warp (quadrant q, k half kh): lane = weight row 32q + lane = its TMEM
     // lane; per half stage it writes k [64kh, 64kh + 64) of that row.
-    const int dw = warp - kWarpDeq;
+    const int dw = warp - R::kWarpDeq;
     const int q = warp & 3, kh = dw >> 2;
     const int row = 32 * q + lane;
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(32 * q) << 16) + kh * 32;
@@ -411,7 +419,7 @@ __global__ void __launch_bounds__(kThreads, NM == 16 ? 2 : 1)
   float acc[NM];
 #pragma unroll
   for (int m = 0; m < NM; ++m) acc[m] = 0.f;
-  if (warp >= kWarpAcc) {
+  if (warp >= R::kWarpAcc) {
     const int q = warp & 3;
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(32 * q) << 16) + kDCol;
     int e = 0;
@@ -424,13 +432,16 @@ __global__ void __launch_bounds__(kThreads, NM == 16 ? 2 : 1)
       const int* ex = exps + e * kMaxRows;
 #pragma unroll
       for (int half = 0; half < NM / 16; ++half) {
-        uint32_t d[16];
-        tmem_ld_16cols(t_lane + dbuf * NM + 16 * half, d);
+        // the two half-stage accumulators of this stage, columns [16 half, +16)
+        uint32_t d0[16], d1[16];
+        tmem_ld_16cols(t_lane + (2 * dbuf) * NM + 16 * half, d0);
+        tmem_ld_16cols(t_lane + (2 * dbuf + 1) * NM + 16 * half, d1);
         tmem_ld_wait();
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
           const int m = 16 * half + j;
-          if (m < M) acc[m] = fmaf(__uint_as_float(d[j]), pow2f(-ex[m]), acc[m]);
+          if (m < M)
+            acc[m] = fmaf(__uint_as_float(d0[j]) + __uint_as_float(d1[j]), pow2f(-ex[m]), acc[m]);
         }
       }
       tc_fence_before_sync();
@@ -445,12 +456,12 @@ __global__ void __launch_bounds__(kThreads, NM == 16 ? 2 : 1)
   // ring for the partial sums [128 rows][NM].
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == kWarpMma) {
+  if (warp == R::kWarpMma) {
     tc_fence_after_sync();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc(tmem, R::kTmemCols);
   }
   float* part = reinterpret_cast<float*>(smem);
-  if (warp >= kWarpAcc) {
+  if (warp >= R::kWarpAcc) {
     const int row = 32 * (warp & 3) + lane;
 #pragma unroll
     for (int m = 0; m < NM; ++m)

@@ -23,6 +23,7 @@ namespace gt = nvfp4::gemvtc;
 // weight bytes an SM should keep in flight (HBM latency x its bandwidth share).
 constexpr double kGroupBytesPerStage = 16.0 * (256 / 2 + 256 / 16);
 constexpr double kWantInFlight = 128.0 * 1024;
+constexpr double kLoneCtaEfficiency = 0.74;
 
 // Bits set by kernels when a pipeline wait gives up (see ptx.cuh).
 __device__ unsigned int g_device_error;
@@ -324,6 +325,9 @@ SmallmPlan plan_smallm(const DeviceInfo& d, int64_t M, int64_t N, int64_t K,
                                  (stages - 1) * g * kGroupBytesPerStage;
         double cost = static_cast<double>(per_sm) * g * ((T + s - 1) / s + 2);
         if (in_flight < kWantInFlight) cost *= kWantInFlight / in_flight;
+        // A lone CTA on an SM issues ~26% slower than two sharing it (fewer
+        // warps to hide latency; measured on the decode shape).
+        if (std::min<int64_t>(per_sm, occ) < 2) cost /= kLoneCtaEfficiency;
         const bool better =
             best_cost < 0 || (one_wave && !best_one_wave) ||
             (one_wave == best_one_wave &&
@@ -425,7 +429,7 @@ GemvPlan plan_gemv(const DeviceInfo& d, int64_t M, int64_t N, int64_t K, unsigne
   for (int s = 2; s <= 8; ++s) {
     const gt::SmemLayout lay = gt::make_layout(NM, static_cast<int>(M), s);
     if (lay.total > d.max_smem || !gt::layout_ok(lay, NM)) continue;
-    const int o = resident_ctas(d, gt::kThreads, regs, lay.total);
+    const int o = resident_ctas(d, gt::Roles<NM>::kThreads, regs, lay.total);
     if (o > occ || (o == occ && o > 0)) {
       occ = o;
       stages = s;
@@ -489,7 +493,7 @@ int launch_gemv(const DeviceInfo& d, const void* x, const uint8_t* wp, const uin
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof cfg);
   cfg.gridDim = dim3(static_cast<unsigned>(plan.row_blocks), static_cast<unsigned>(plan.split), 1);
-  cfg.blockDim = dim3(gt::kThreads, 1, 1);
+  cfg.blockDim = dim3(gt::Roles<NM>::kThreads, 1, 1);
   cfg.dynamicSmemBytes = p.lay.total;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
