@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <climits>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -24,6 +25,7 @@ namespace gt = nvfp4::gemvtc;
 constexpr double kGroupBytesPerStage = 16.0 * (256 / 2 + 256 / 16);
 constexpr double kWantInFlight = 128.0 * 1024;
 constexpr double kLoneCtaEfficiency = 0.74;
+constexpr int kTcgemmTilesPerCta = 4;
 
 // Bits set by kernels when a pipeline wait gives up (see ptx.cuh).
 __device__ unsigned int g_device_error;
@@ -535,10 +537,15 @@ int launch_tcgemm(const DeviceInfo& d, const void* x, const uint8_t* wp, const u
   p.out_f32 = (flags & NVFP4_FLAG_F32_OUT) ? 1 : 0;
   p.swiglu = swiglu ? 1 : 0;
   p.err = d.err;
+  const int64_t tiles_w = swiglu ? (N / 2) / 64 : N / T::kTileW;
+  const int64_t tiles_x = (M + T::kTileX - 1) / T::kTileX;
+  if (tiles_w * tiles_x > INT32_MAX) return NVFP4_ERR_SHAPE;
+  p.tiles_w = static_cast<int>(tiles_w);
+  p.tiles_total = static_cast<int>(tiles_w * tiles_x);
+  p.tiles_per_cta = kTcgemmTilesPerCta;
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof cfg);
-  cfg.gridDim = dim3(static_cast<unsigned>(swiglu ? (N / 2) / 64 : N / T::kTileW),
-                     static_cast<unsigned>((M + T::kTileX - 1) / T::kTileX), 1);
+  cfg.gridDim = dim3(static_cast<unsigned>((p.tiles_total + p.tiles_per_cta - 1) / p.tiles_per_cta), 1, 1);
   cfg.blockDim = dim3(T::kThreads, 1, 1);
   cfg.dynamicSmemBytes = T::kSmemBytes;
   cfg.stream = stream;

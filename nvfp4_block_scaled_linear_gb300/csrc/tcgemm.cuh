@@ -10,14 +10,20 @@
 // the other orientation.  D = W x^T sits in TMEM as 128 lanes (weight rows)
 // x 256 f32 columns (activation rows).
 //
-// Warp roles (320 threads):
+// Persistent: one CTA per SM walks the output tiles (activation tiles
+// outermost, so that a wave of CTAs shares one activation tile in L2), and
+// the accumulator is double-buffered in TMEM (2 x 256 columns) so that the
+// epilogue of one tile overlaps the k loop of the next.
+//
+// Warp roles (448 threads):
 //   warp 0      TMA producer: activation tile (128B-swizzled, the B operand
 //               as-is), packed weights (32B-swizzled) and block scales;
 //   warp 1      TMEM allocation and the single MMA-issuing thread;
 //   warps 2..9  dequantise packed weights to bf16 straight into the A
-//               operand's 128B-swizzled K-major layout; after the k loop
-//               they drain TMEM (tcgen05.ld), apply 2^10 / global_scale and
-//               the optional SwiGLU, and store bf16 (or f32).
+//               operand's 128B-swizzled K-major layout;
+//   warps 10..13 epilogue: drain a finished accumulator (tcgen05.ld), apply
+//               2^10 / global_scale and the optional SwiGLU, store bf16 (or
+//               f32), and hand the accumulator back to the MMA issuer.
 // All waits are mbarrier waits with a time limit (see ptx.cuh).
 #pragma once
 #include <cstdint>
@@ -35,7 +41,10 @@ constexpr int kStageK = 64;                 // k per stage (one 128 B swizzle ro
 constexpr int kUmmaK = 16;
 constexpr int kStages = 4;
 constexpr int kDequantWarps = 8;
-constexpr int kThreads = (2 + kDequantWarps) * 32;
+constexpr int kEpiWarps = 4;
+constexpr int kWarpDeq = 2;
+constexpr int kWarpEpi = kWarpDeq + kDequantWarps;     // 10
+constexpr int kThreads = (kWarpEpi + kEpiWarps) * 32;  // 448
 constexpr int kXBytes = kTileX * kStageK * 2;          // 32 KB
 constexpr int kABytes = kTileW * kStageK * 2;          // 16 KB
 constexpr int kRawBytes = kTileW * kStageK / 2;        // 4 KB
@@ -48,9 +57,10 @@ constexpr int kStageBytes = kSclOff + kSclBytes;      // 54 KB, 1024-multiple
 constexpr int kTxBytes = kXBytes + kRawBytes + kSclBytes;
 constexpr int kLutOff = kStages * kStageBytes;
 constexpr int kBarOff = kLutOff + 256 * 4;
-constexpr int kNumBars = 3 * kStages + 1;
+constexpr int kNumBars = 3 * kStages + 5;
 constexpr int kSmemBytes = kBarOff + kNumBars * 8 + 16 + 1024;
-constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kAccCols = 256;          // one accumulator: 256 f32 columns
+constexpr uint32_t kTmemCols = 2 * kAccCols;  // double-buffered
 static_assert(kStageBytes % 1024 == 0, "stages must keep 1024-byte alignment");
 
 struct Params {
@@ -59,6 +69,9 @@ struct Params {
   float out_scale;      // fp32(2^10 / global_scale)
   int out_f32;
   int swiglu;          // tile = 64 gate rows + the 64 matching up rows
+  int tiles_w;         // weight tiles (N / 128)
+  int tiles_total;     // weight tiles x activation tiles
+  int tiles_per_cta;   // consecutive tiles each CTA takes
   unsigned int* err;
 };
 
@@ -73,23 +86,33 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* tma_full = reinterpret_cast<uint64_t*>(smem + kBarOff);
   uint64_t* a_full = tma_full + kStages;
   uint64_t* empty = a_full + kStages;
-  uint64_t* acc_full = empty + kStages;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(acc_full + 1);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1) + 1;
+  uint64_t* acc_full = empty + kStages;      // [2] accumulator b holds a finished tile
+  uint64_t* acc_empty = acc_full + 2;        // [2] accumulator b drained by the epilogue
+  uint64_t* mma_done = acc_empty + 2;        // every MMA issued has completed
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(mma_done + 1);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1) + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_stages = static_cast<int>(p.K / kStageK);
-  const int m_tile = blockIdx.y * kTileX;
-  const int bw = blockIdx.x;
-  // weight rows feeding A rows [0,64) and [64,128)
-  int wrow0, wrow1;
-  if (p.swiglu) {
-    wrow0 = bw * 64;                                   // gate rows
-    wrow1 = static_cast<int>(p.N / 2) + bw * 64;       // matching up rows
-  } else {
-    wrow0 = bw * kTileW;
-    wrow1 = wrow0 + 64;
-  }
+  // This CTA's tiles: t = blockIdx.x * tiles_per_cta + i, i < my_tiles;
+  // tile t = (weight tile t % tiles_w, activation tile t / tiles_w).
+  const int t0 = blockIdx.x * p.tiles_per_cta;
+  const int my_tiles = min(p.tiles_per_cta, p.tiles_total - t0);
+  auto tile_of = [&](int i, int& bw, int& m_tile) {
+    const int t = t0 + i;
+    bw = t % p.tiles_w;
+    m_tile = (t / p.tiles_w) * kTileX;
+  };
+  // weight rows feeding A rows [0,64) and [64,128) of weight tile bw
+  auto wrows = [&](int bw, int& wrow0, int& wrow1) {
+    if (p.swiglu) {
+      wrow0 = bw * 64;                                   // gate rows
+      wrow1 = static_cast<int>(p.N / 2) + bw * 64;       // matching up rows
+    } else {
+      wrow0 = bw * kTileW;
+      wrow1 = wrow0 + 64;
+    }
+  };
 
   for (int i = threadIdx.x; i < 256; i += kThreads) lut[i] = scale_pair_from_e4m3(i);
   if (threadIdx.x == 0) {
@@ -98,7 +121,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&a_full[s], kDequantWarps);
       mbar_init(&empty[s], 1);
     }
-    mbar_init(acc_full, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&acc_full[b], 1);
+      mbar_init(&acc_empty[b], kEpiWarps);
+    }
+    mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -109,7 +136,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
-  const uint32_t tmem_acc = *tmem_slot;
+  const uint32_t tmem_base = *tmem_slot;
+  // One CTA per SM: a dependent kernel's CTAs only start as these exit.
+  if (threadIdx.x == 0) griddep_launch_dependents();
+  const int total_stages = my_tiles * n_stages;
 
   if (warp == 0) {
     // ---------------------------------------------------------- TMA producer
@@ -118,43 +148,74 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tensormap(&tm_w);
       prefetch_tensormap(&tm_s);
       const uint64_t pol_w = policy_evict_last();    // weights: reused by M tiles
-      auto issue_weights = [&](int it, int slot) {
+      // Cursor over (tile i, stage it): the single producer thread must not
+      // spend its stage budget on divisions, so tile coordinates change only
+      // at tile boundaries.
+      struct Cursor {
+        int i, it, m_tile, wrow0, wrow1;
+      };
+      auto start_tile = [&](Cursor& c) {
+        int bw;
+        tile_of(c.i, bw, c.m_tile);
+        wrows(bw, c.wrow0, c.wrow1);
+      };
+      auto advance = [&](Cursor& c) {
+        if (++c.it == n_stages) {
+          c.it = 0;
+          if (++c.i < my_tiles) start_tile(c);
+        }
+      };
+      auto issue_weights = [&](const Cursor& c, int slot) {
         uint8_t* st = smem + slot * kStageBytes;
-        const int k0 = it * kStageK;
-        tma_load_2d_hint(st + kRawOff, &tm_w, &tma_full[slot], k0 / 2, wrow0, pol_w);
-        tma_load_2d_hint(st + kRawOff + kRawBytes / 2, &tm_w, &tma_full[slot], k0 / 2, wrow1,
+        const int k0 = c.it * kStageK;
+        tma_load_2d_hint(st + kRawOff, &tm_w, &tma_full[slot], k0 / 2, c.wrow0, pol_w);
+        tma_load_2d_hint(st + kRawOff + kRawBytes / 2, &tm_w, &tma_full[slot], k0 / 2, c.wrow1,
                          pol_w);
         const int sx = (k0 / 16) & ~15;
-        tma_load_2d_hint(st + kSclOff, &tm_s, &tma_full[slot], sx, wrow0, pol_w);
-        tma_load_2d_hint(st + kSclOff + kSclBytes / 2, &tm_s, &tma_full[slot], sx, wrow1,
+        tma_load_2d_hint(st + kSclOff, &tm_s, &tma_full[slot], sx, c.wrow0, pol_w);
+        tma_load_2d_hint(st + kSclOff + kSclBytes / 2, &tm_s, &tma_full[slot], sx, c.wrow1,
                          pol_w);
       };
-      auto issue_acts = [&](int it, int slot) {
-        tma_load_2d(smem + slot * kStageBytes + kXOff, &tm_x, &tma_full[slot], it * kStageK,
-                    m_tile);
+      auto issue_acts = [&](const Cursor& c, int slot) {
+        tma_load_2d(smem + slot * kStageBytes + kXOff, &tm_x, &tma_full[slot], c.it * kStageK,
+                    c.m_tile);
       };
+      Cursor cur{0, 0, 0, 0, 0};
+      if (my_tiles > 0) start_tile(cur);
       // Weights first (independent of the preceding kernel in the stream),
       // activations after the programmatic-dependent-launch wait.
-      const int pre = n_stages < kStages ? n_stages : kStages;
-      for (int it = 0; it < pre; ++it) {
-        mbar_arrive_expect_tx(&tma_full[it], kTxBytes);
-        issue_weights(it, it);
+      const int pre = total_stages < kStages ? total_stages : kStages;
+      const Cursor first_cur = cur;
+      for (int g = 0; g < pre; ++g) {
+        mbar_arrive_expect_tx(&tma_full[g], kTxBytes);
+        issue_weights(cur, g);
+        advance(cur);
       }
       griddep_wait();
-      for (int it = 0; it < pre; ++it) issue_acts(it, it);
+      Cursor acts_cur = first_cur;
+      for (int g = 0; g < pre; ++g) {
+        issue_acts(acts_cur, g);
+        advance(acts_cur);
+      }
       int issued = pre;
-      for (int it = pre; it < n_stages; ++it) {
-        const int slot = it % kStages;
-        if (!mbar_wait(&empty[slot], ((it / kStages) & 1) ^ 1, abort_flag)) break;
+      int slot = pre == kStages ? 0 : pre;
+      uint32_t par = pre == kStages ? 0u : 1u;
+      for (int g = pre; g < total_stages; ++g) {
+        if (!mbar_wait(&empty[slot], par, abort_flag)) break;
         mbar_arrive_expect_tx(&tma_full[slot], kTxBytes);
-        issue_weights(it, slot);
-        issue_acts(it, slot);
+        issue_weights(cur, slot);
+        issue_acts(cur, slot);
+        advance(cur);
         ++issued;
+        if (++slot == kStages) {
+          slot = 0;
+          par ^= 1u;
+        }
       }
       const int first = issued > kStages ? issued - kStages : 0;
-      for (int it = first; it < issued; ++it) {
+      for (int g = first; g < issued; ++g) {
         volatile int no_abort = 0;
-        if (!mbar_wait(&tma_full[it % kStages], (it / kStages) & 1, &no_abort))
+        if (!mbar_wait(&tma_full[g % kStages], (g / kStages) & 1, &no_abort))
           atomicOr(p.err, kErrWaitTimeout);
       }
     }
@@ -163,36 +224,55 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc = umma_idesc_bf16(kTileW, kTileX);
       bool ok = true;
-      for (int it = 0; it < n_stages && ok; ++it) {
-        const int slot = it % kStages;
-        const uint32_t par = (it / kStages) & 1;
-        ok = mbar_wait(&tma_full[slot], par, abort_flag) &&
-             mbar_wait(&a_full[slot], par, abort_flag);
+      int slot = 0;
+      uint32_t par = 0;
+      for (int i = 0; i < my_tiles && ok; ++i) {
+        const int b = i & 1;
+        // the epilogue has drained accumulator b (tile i - 2)
+        ok = mbar_wait(&acc_empty[b], ((i >> 1) & 1) ^ 1u, abort_flag);
         if (!ok) break;
         tc_fence_after_sync();
-        const uint32_t st = smem_addr(smem + slot * kStageBytes);
+        const uint32_t tmem_acc = tmem_base + b * kAccCols;
+        for (int it = 0; it < n_stages; ++it) {
+          ok = mbar_wait(&tma_full[slot], par, abort_flag) &&
+               mbar_wait(&a_full[slot], par, abort_flag);
+          if (!ok) break;
+          tc_fence_after_sync();
+          const uint32_t st = smem_addr(smem + slot * kStageBytes);
 #pragma unroll
-        for (int kk = 0; kk < kStageK / kUmmaK; ++kk) {
-          const uint64_t a_desc = umma_desc_sw128(st + kAOff + kk * kUmmaK * 2);
-          const uint64_t b_desc = umma_desc_sw128(st + kXOff + kk * kUmmaK * 2);
-          umma_bf16(tmem_acc, a_desc, b_desc, idesc, (it | kk) != 0);
+          for (int kk = 0; kk < kStageK / kUmmaK; ++kk) {
+            const uint64_t a_desc = umma_desc_sw128(st + kAOff + kk * kUmmaK * 2);
+            const uint64_t b_desc = umma_desc_sw128(st + kXOff + kk * kUmmaK * 2);
+            umma_bf16(tmem_acc, a_desc, b_desc, idesc, (it | kk) != 0);
+          }
+          umma_commit(&empty[slot]);
+          if (++slot == kStages) {
+            slot = 0;
+            par ^= 1u;
+          }
         }
-        umma_commit(&empty[slot]);
+        if (ok) umma_commit(&acc_full[b]);
       }
-      umma_commit(acc_full);
+      // Every MMA issued must have completed before TMEM is released.
+      umma_commit(mma_done);
+      volatile int no_abort = 0;
+      if (!mbar_wait(mma_done, 0, &no_abort)) atomicOr(p.err, kErrWaitTimeout);
     }
-  } else {
+  } else if (warp < kWarpEpi) {
     // ---------------------------------------------------------- dequantisers
-    const int d = warp - 2;                       // 0..7
-    const int r = (d & 3) * 32 + lane;            // raw weight row in the tile
+    const int d = warp - kWarpDeq;                // 0..7
     const int h = d >> 2;                         // k half: [32h, 32h+32)
-    // A row: identity, or interleaved gate/up pairs (2j gate, 2j+1 up) so
-    // that one warp holds both halves of every SwiGLU output.
-    const int arow = p.swiglu ? (r < 64 ? 2 * r : 2 * (r - 64) + 1) : r;
+    // A row (= TMEM lane) written by this thread: consecutive across the
+    // warp, so that the swizzled shared-memory stores are conflict free.
+    // SwiGLU interleaves gate/up pairs (A row 2j = gate row j, 2j+1 = up
+    // row j) so that one warp holds both halves of every output.
+    const int arow = (d & 3) * 32 + lane;
+    const int r = p.swiglu ? ((arow & 1) ? 64 + (arow >> 1) : (arow >> 1)) : arow;  // raw row
     const uint32_t a_row_off = (arow >> 3) * 1024 + (arow & 7) * 128;
-    for (int it = 0; it < n_stages; ++it) {
-      const int slot = it % kStages;
-      if (!mbar_wait(&tma_full[slot], (it / kStages) & 1, abort_flag)) break;
+    int slot = 0, it = 0;
+    uint32_t par = 0;
+    for (int g = 0; g < total_stages; ++g, it = (it + 1 == n_stages) ? 0 : it + 1) {
+      if (!mbar_wait(&tma_full[slot], par, abort_flag)) break;
       uint8_t* st = smem + slot * kStageBytes;
       const uint4 raw = *reinterpret_cast<const uint4*>(
           st + kRawOff + r * 32 + ((h ^ ((r >> 2) & 1)) << 4));
@@ -212,32 +292,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&a_full[slot]);
+      if (++slot == kStages) {
+        slot = 0;
+        par ^= 1u;
+      }
     }
-
+  } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;                       // TMEM lane quarter
-    const int colhalf = d >> 2;                   // activation rows [128c, 128c+128)
-    if (warp == 2 && lane == 0) griddep_launch_dependents();
-    // Warp-uniform (and reconverged) before the warp-aligned tcgen05.ld.
-    const bool have_acc = __all_sync(0xffffffffu, mbar_wait(acc_full, 0, abort_flag));
-    tc_fence_after_sync();
-    if (have_acc) {
-      const int lane_row = 32 * q + lane;         // A row = TMEM lane
-      const int64_t n_out = p.swiglu ? p.N / 2 : p.N;
-      int64_t ncol;
-      if (p.swiglu)
-        ncol = static_cast<int64_t>(bw) * 64 + (lane_row >> 1);
-      else
-        ncol = static_cast<int64_t>(bw) * kTileW + lane_row;
+    const int lane_row = 32 * q + lane;           // A row = TMEM lane
+    const int64_t n_out = p.swiglu ? p.N / 2 : p.N;
+    for (int i = 0; i < my_tiles; ++i) {
+      const int b = i & 1;
+      // Warp-uniform (and reconverged) before the warp-aligned tcgen05.ld.
+      if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[b], (i >> 1) & 1, abort_flag))) break;
+      tc_fence_after_sync();
+      int bw, m_tile;
+      tile_of(i, bw, m_tile);
+      const int64_t ncol = p.swiglu ? static_cast<int64_t>(bw) * 64 + (lane_row >> 1)
+                                    : static_cast<int64_t>(bw) * kTileW + lane_row;
+      const uint32_t t_acc = tmem_base + b * kAccCols + (static_cast<uint32_t>(32 * q) << 16);
 #pragma unroll 1
-      for (int c0 = colhalf * 128; c0 < colhalf * 128 + 128; c0 += 32) {
+      for (int c0 = 0; c0 < kTileX; c0 += 32) {
         uint32_t v[32];
-        tmem_ld_32cols(tmem_acc + (static_cast<uint32_t>(32 * q) << 16) + c0, v);
+        tmem_ld_32cols(t_acc + c0, v);
         tmem_ld_wait();
+        if (c0 + 32 == kTileX) {
+          // the accumulator is read out: the MMA issuer may reuse it
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_empty[b]);
+        }
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int m = m_tile + c0 + i;
-          float yv = __uint_as_float(v[i]) * p.out_scale;
+        for (int j = 0; j < 32; ++j) {
+          const int m = m_tile + c0 + j;
+          float yv = __uint_as_float(v[j]) * p.out_scale;
           if (p.swiglu) {
             const float up = __shfl_xor_sync(0xffffffffu, yv, 1);
             yv = silu_mul(yv, up);
@@ -260,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after_sync();
-    tmem_dealloc(tmem_acc, kTmemCols);
+    tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
