@@ -33,9 +33,9 @@ namespace nvfp4 {
 constexpr float kWeightPow2 = 1024.0f;   // 2^10
 
 // SwiGLU epilogue: silu(g) * u = g / (1 + e^-g) * u, in fp32 with the CUDA
-// fast exponential and a correctly rounded reciprocal (e^-g = inf gives 0).
+// fast exponential and fast division (a few ulp; e^-g = inf gives 0).
 __device__ __forceinline__ float silu_mul(float g, float u) {
-  return g * __frcp_rn(1.0f + __expf(-g)) * u;
+  return __fdividef(g, 1.0f + __expf(-g)) * u;
 }
 
 // bf16x2 (S, S) for an e4m3 bit pattern, S = value * 2^116; NaN for S.1111.111.

@@ -328,12 +328,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int m = m_tile + c0 + j;
           float yv = __uint_as_float(v[j]) * p.out_scale;
           if (p.swiglu) {
-            const float up = __shfl_xor_sync(0xffffffffu, yv, 1);
-            yv = silu_mul(yv, up);
-            if ((lane & 1) || m >= p.M) continue;
-          } else if (m >= p.M) {
-            continue;
+            // lanes 2k (gate) and 2k+1 (up) share output column ncol; the
+            // even lane takes the even activation rows, the odd lane the odd
+            const float other = __shfl_xor_sync(0xffffffffu, yv, 1);
+            if ((j & 1) != (lane & 1)) continue;
+            yv = (lane & 1) ? silu_mul(other, yv) : silu_mul(yv, other);
           }
+          if (m >= p.M) continue;
           const int64_t off = static_cast<int64_t>(m) * n_out + ncol;
           if (p.out_f32)
             static_cast<float*>(p.y)[off] = yv;
