@@ -93,7 +93,7 @@ struct SmemLayout {
   int total;        // dynamic shared memory to request (with alignment slack)
 };
 
-__host__ __device__ constexpr int num_barriers(int stages) { return 5 * stages + 12; }
+__host__ __device__ constexpr int num_barriers(int stages) { return 5 * stages + 7; }
 
 __host__ __device__ constexpr SmemLayout make_layout(int n_mma, int m_rows, int stages) {
   SmemLayout l{};
@@ -159,13 +159,16 @@ __global__ void __launch_bounds__(Roles<NM>::kThreads, NM == 16 ? 2 : 1)
   uint32_t* lut = reinterpret_cast<uint32_t*>(smem + L.lut_off);
   int* exps = reinterpret_cast<int*>(smem + L.exp_off);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bar_off);   // TMA landed
-  uint64_t* empty = full + S;          // stage consumed (both issuers' commits)
+  // stage consumed: both issuers' MMAs of the stage have completed (their one
+  // commit each).  Besides releasing the ring slot, it tells the accumulator
+  // warps that the stage's D is ready and the dequantisers that the stage's
+  // TMEM weight slots are free: one tcgen05.commit per stage and issuer
+  // (a commit costs the issuing thread far more than an MMA).
+  uint64_t* empty = full + S;
   uint64_t* b_full = empty + S;        // f16 activations written (converters)
   uint64_t* exp_full = b_full + S;     // [2S] exponents written (converters)
   uint64_t* a_full = exp_full + 2 * S; // [3] TMEM weights written (dequantisers)
-  uint64_t* a_empty = a_full + kASlots;    // [3] TMEM weights consumed (MMA commit)
-  uint64_t* d_full = a_empty + kASlots;    // [2] stage accumulators ready (both issuers)
-  uint64_t* d_empty = d_full + 2;          // [2] stage accumulators read (acc warps)
+  uint64_t* d_empty = a_full + kASlots;    // [2] stage accumulators read (acc warps)
   uint64_t* mma_done = d_empty + 2;        // [2] every MMA of issuer h has completed
   volatile int* abort_flag = reinterpret_cast<volatile int*>(mma_done + 2);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 2) + 1;
@@ -203,12 +206,8 @@ __global__ void __launch_bounds__(Roles<NM>::kThreads, NM == 16 ? 2 : 1)
       mbar_init(&b_full[s], R::kConvWarps);
     }
     for (int e = 0; e < 2 * S; ++e) mbar_init(&exp_full[e], R::kConvWarps);
-    for (int a = 0; a < kASlots; ++a) {
-      mbar_init(&a_full[a], R::kDeqWarps);
-      mbar_init(&a_empty[a], 1);
-    }
+    for (int a = 0; a < kASlots; ++a) mbar_init(&a_full[a], R::kDeqWarps);
     for (int d = 0; d < 2; ++d) {
-      mbar_init(&d_full[d], 2);
       mbar_init(&d_empty[d], R::kAccWarps);
       mbar_init(&mma_done[d], 1);
     }
@@ -312,9 +311,7 @@ __global__ void __launch_bounds__(Roles<NM>::kThreads, NM == 16 ? 2 : 1)
               b_desc0 + static_cast<uint64_t>(((kk / 4) * (NM * 128) + (kk % 4) * 32) >> 4);
           umma_f16_tmem_a(d_tmem, a_tmem + kk * 8, b_desc, idesc, kk != 0);
         }
-        umma_commit(&a_empty[aslot]);
         umma_commit(&empty[slot]);
-        umma_commit(&d_full[dbuf]);
         slot = next_slot(slot, S, par);
       }
       // Every MMA issued must have completed before TMEM is released.
@@ -335,24 +332,41 @@ __global__ void __launch_bounds__(Roles<NM>::kThreads, NM == 16 ? 2 : 1)
     for (int it = 0; it < n_stages; ++it) {
       if (!warp_wait(&full[slot], par, abort_flag)) break;
       uint8_t* st = smem + slot * L.stage_bytes;
-      for (int m = c; m < M; m += R::kConvWarps) {
-        const uint4 v = *reinterpret_cast<const uint4*>(st + L.x_off + m * 512 + lane * 16);
-        uint32_t mx = max_u16x2(max_u16x2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
-                                max_u16x2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
-        mx = __reduce_max_sync(0xffffffffu, max(mx & 0xFFFFu, mx >> 16));
-        const int e_max = static_cast<int>(mx >> 7);           // biased bf16 exponent
-        const int a = min(126, max(-126, 141 - e_max));        // max * 2^a < 2^15
-        const float f = pow2f(a);
-        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-        uint32_t o[4];
+      // four rows at a time: their load -> max -> scale -> store chains
+      // overlap (one row at a time leaves the warp waiting on latencies)
+      for (int m0 = c; m0 < M; m0 += 4 * R::kConvWarps) {
+        uint4 v[4];
+        int e_max[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          o[j] = f32x2_to_f16x2(__uint_as_float(w4[j] << 16) * f,
-                                __uint_as_float(w4[j] & 0xFFFF0000u) * f);
-        *reinterpret_cast<uint4*>(st + L.b_off + q * (NM * 128) + (m >> 3) * 1024 +
-                                  (m & 7) * 128 + ((c16 ^ (m & 7)) << 4)) =
-            make_uint4(o[0], o[1], o[2], o[3]);
-        if (lane == 0) exps[e * kMaxRows + m] = a;
+        for (int u = 0; u < 4; ++u) {
+          const int m = m0 + u * R::kConvWarps;
+          v[u] = m < M ? *reinterpret_cast<const uint4*>(st + L.x_off + m * 512 + lane * 16)
+                       : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          uint32_t mx = max_u16x2(max_u16x2(v[u].x & 0x7FFF7FFFu, v[u].y & 0x7FFF7FFFu),
+                                  max_u16x2(v[u].z & 0x7FFF7FFFu, v[u].w & 0x7FFF7FFFu));
+          mx = __reduce_max_sync(0xffffffffu, max(mx & 0xFFFFu, mx >> 16));
+          e_max[u] = static_cast<int>(mx >> 7);                 // biased bf16 exponent
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int m = m0 + u * R::kConvWarps;
+          if (m >= M) break;
+          const int a = min(126, max(-126, 141 - e_max[u]));    // max * 2^a < 2^15
+          const float f = pow2f(a);
+          const uint32_t w4[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+          uint32_t o[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            o[j] = f32x2_to_f16x2(__uint_as_float(w4[j] << 16) * f,
+                                  __uint_as_float(w4[j] & 0xFFFF0000u) * f);
+          *reinterpret_cast<uint4*>(st + L.b_off + q * (NM * 128) + (m >> 3) * 1024 +
+                                    (m & 7) * 128 + ((c16 ^ (m & 7)) << 4)) =
+              make_uint4(o[0], o[1], o[2], o[3]);
+          if (lane == 0) exps[e * kMaxRows + m] = a;
+        }
       }
       fence_proxy_async_smem();      // the operand, for the tensor core
       __syncwarp();
@@ -372,7 +386,11 @@ __global__ void __launch_bounds__(Roles<NM>::kThreads, NM == 16 ? 2 : 1)
     const int row = 32 * q + lane;
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(32 * q) << 16) + kh * 32;
     int slot = 0, aslot = 0;
-    uint32_t par = 0, apar = 0;
+    uint32_t par = 0;
+    // Half stage g reuses the TMEM slot of half g - 3, whose stage
+    // (g - 3) / 2 must have completed: `done_*` walks those stages.
+    int done_slot = 0;
+    uint32_t done_par = 0;
     bool ok = true;
     for (int it = 0; it < n_stages && ok; ++it) {
       if (!warp_wait(&full[slot], par, abort_flag)) break;
@@ -380,9 +398,14 @@ __global__ void __launch_bounds__(Roles<NM>::kThreads, NM == 16 ? 2 : 1)
       const uint4 sc = *reinterpret_cast<const uint4*>(st + L.s_off + row * 16);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        if (!warp_wait(&a_empty[aslot], apar ^ 1u, abort_flag)) {
-          ok = false;
-          break;
+        const int g = 2 * it + h;
+        if (g >= kASlots) {
+          if (!warp_wait(&empty[done_slot], done_par, abort_flag)) {
+            ok = false;
+            break;
+          }
+          // g - 3 odd: the next half (g + 1) waits on the same stage
+          if ((g - kASlots) & 1) done_slot = next_slot(done_slot, S, done_par);
         }
         // 64 k = two 16-byte code chunks of the row's 128-byte line
         const int c0 = 4 * h + 2 * kh;
@@ -402,12 +425,13 @@ __global__ void __launch_bounds__(Roles<NM>::kThreads, NM == 16 ? 2 : 1)
         dequant8_f16(w1.y, S2, &out[20]);
         dequant8_f16(w1.z, S3, &out[24]);
         dequant8_f16(w1.w, S3, &out[28]);
+        tc_fence_after_sync();
         tmem_st_32cols(t_lane + aslot * kAColsPerSlot, out);
         tmem_st_wait();
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(&a_full[aslot]);
-        aslot = next_slot(aslot, kASlots, apar);
+        aslot = aslot + 1 == kASlots ? 0 : aslot + 1;
       }
       slot = next_slot(slot, S, par);
     }
@@ -422,11 +446,13 @@ __global__ void __launch_bounds__(Roles<NM>::kThreads, NM == 16 ? 2 : 1)
   if (warp >= R::kWarpAcc) {
     const int q = warp & 3;
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(32 * q) << 16) + kDCol;
-    int e = 0;
-    uint32_t epar = 0;
+    int e = 0, slot = 0;
+    uint32_t epar = 0, par = 0;
     for (int it = 0; it < n_stages; ++it) {
       const int dbuf = it & 1;
-      if (!warp_wait(&d_full[dbuf], (it >> 1) & 1, abort_flag)) break;
+      // the stage's MMAs have completed: its accumulators are ready
+      if (!warp_wait(&empty[slot], par, abort_flag)) break;
+      slot = next_slot(slot, S, par);
       if (!warp_wait(&exp_full[e], epar, abort_flag)) break;
       tc_fence_after_sync();
       const int* ex = exps + e * kMaxRows;
