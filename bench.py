@@ -334,37 +334,36 @@ def time_case(case, steps, warmup, stream, world, sampler=None, graph=True):
 
 
 def e2e_case(case, steps, stream, dev):
-    """Same workload through the public API with host buffers: pinned host
-    inputs copied in, the call, the result copied out -- all timed."""
+    """Same workload through the public API (the eager Python call) with the
+    step's data in host memory: every step copies its activations in from
+    pinned host memory, calls the layer and copies its result out to pinned
+    host memory, all inside the timed region.  The packed weights and scales
+    are the model's resident parameters (rotated over the same copies as the
+    device-timed loop, so they stream from HBM), not step inputs."""
     import torch
     hx = [x.cpu().pin_memory() for x in case.x]
-    hwp = [w.cpu().pin_memory() for w in case.wp[0]]
-    hws = [w.cpu().pin_memory() for w in case.ws[0]]
     hy = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for y in case.y]
     dx = [torch.empty_like(x) for x in case.x]
-    dwp = [torch.empty_like(w) for w in case.wp[0]]
-    dws = [torch.empty_like(w) for w in case.ws[0]]
-    h2d = sum(t.nbytes for t in hx + hwp + hws)
+    h2d = sum(t.nbytes for t in hx)
     d2h = sum(t.nbytes for t in hy)
 
-    def one():
+    def one(i):
+        c = i % case.copies
         with torch.cuda.stream(stream):
             for j, t in enumerate(case.linears):
                 dx[j].copy_(hx[j], non_blocking=True)
-                dwp[j].copy_(hwp[j], non_blocking=True)
-                dws[j].copy_(hws[j], non_blocking=True)
-                case.lib.linear_ex(dx[j], dwp[j], dws[j], float(t.global_scale), case.flags,
-                                   out=case.y[j], stream=stream)
+                case.lib.linear_ex(dx[j], case.wp[c][j], case.ws[c][j], float(t.global_scale),
+                                   case.flags, out=case.y[j], stream=stream)
                 hy[j].copy_(case.y[j], non_blocking=True)
 
-    for _ in range(2):
-        one()
+    for i in range(3):
+        one(i)
     torch.cuda.synchronize()
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
     a.record(stream)
-    for _ in range(steps):
-        one()
+    for i in range(steps):
+        one(i)
     b.record(stream)
     torch.cuda.synchronize()
     ms = a.elapsed_time(b) / steps
@@ -432,7 +431,7 @@ def run_ours(args):
         line["config"]["max_rows"] = args.max_rows
 
     if not args.no_extras:
-        e2e_ms, h2d, d2h = e2e_case(head, max(3, min(20, args.steps)), stream, dev)
+        e2e_ms, h2d, d2h = e2e_case(head, max(3, min(500, args.steps)), stream, dev)
         e2e_val = (head.flops / 1e12 if tensor_bound else head.bytes / 1e9) / (e2e_ms / 1e3)
         line["e2e"] = {"value": round(e2e_val * world, 2), "unit": unit,
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,

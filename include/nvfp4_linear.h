@@ -133,6 +133,17 @@ int nvfp4_linear_swiglu_f32(const void* x, const uint8_t* w_packed,
                             const uint8_t* w_scale, float global_scale, float* y,
                             int64_t M, int64_t N, int64_t K, void* stream);
 
+/* Fused gate/up projection with SwiGLU where the gate rows [0, N/2) and the
+ * up rows [N/2, N) carry their own global scales (a checkpoint whose gate
+ * and up projections were quantised separately, stored as one weight; the
+ * FlashRT docs, section 4, fuse the pair only "when the gate/up scales
+ * allow it" -- here they always can).  Gate results use gate_global_scale,
+ * up results up_global_scale; otherwise as nvfp4_linear_swiglu.  `flags`
+ * may add NVFP4_FLAG_F32_OUT and the kernel and tuning flags below. */
+int nvfp4_linear_swiglu_gs(const void* x, const uint8_t* w_packed, const uint8_t* w_scale,
+                           float gate_global_scale, float up_global_scale, void* y, int64_t M,
+                           int64_t N, int64_t K, unsigned int flags, void* stream);
+
 /* General form of the four calls above; `flags` is an OR of NVFP4_FLAG_*.
  * The FORCE flags pick a kernel regardless of M (for A/B measurements and
  * for checking both kernels on the same inputs). */

@@ -79,6 +79,9 @@ def load_library(path=None):
         f.argtypes = [P, P, P, ctypes.c_float, P, i64, i64, i64, P]
     lib.nvfp4_linear_ex.restype = ctypes.c_int
     lib.nvfp4_linear_ex.argtypes = [P, P, P, ctypes.c_float, P, i64, i64, i64, u32, P]
+    lib.nvfp4_linear_swiglu_gs.restype = ctypes.c_int
+    lib.nvfp4_linear_swiglu_gs.argtypes = [P, P, P, ctypes.c_float, ctypes.c_float, P, i64, i64,
+                                           i64, u32, P]
     lib.nvfp4_linear_kernel_for.restype = ctypes.c_int
     lib.nvfp4_linear_kernel_for.argtypes = [i64, i64, i64, u32]
     lib.nvfp4_device_status.restype = ctypes.c_int
@@ -181,6 +184,29 @@ def linear_swiglu(x, w_packed, w_scale, global_scale, out=None, stream=None):
 def linear_swiglu_f32(x, w_packed, w_scale, global_scale, out=None, stream=None):
     return linear_ex(x, w_packed, w_scale, global_scale, FLAG_SWIGLU | FLAG_F32_OUT, out,
                      stream)
+
+
+def linear_swiglu_gs(x, w_packed, w_scale, gate_global_scale, up_global_scale, flags=0,
+                     out=None, stream=None):
+    """nvfp4_linear_swiglu_gs: SwiGLU with separate gate and up global scales."""
+    w_packed, w_scale, M, N, K = _check(x, w_packed, w_scale)
+    dtype = torch.float32 if flags & FLAG_F32_OUT else torch.bfloat16
+    if out is None:
+        out = torch.empty((M, N // 2), dtype=dtype, device=x.device)
+    elif (out.dtype != dtype or tuple(out.shape) != (M, N // 2) or not out.is_contiguous()
+          or out.device != x.device):
+        raise ValueError("out must be a contiguous %s tensor of shape %s on %s"
+                         % (dtype, (M, N // 2), x.device))
+    if stream is None:
+        stream = torch.cuda.current_stream(x.device)
+    with torch.cuda.device(x.device):
+        st = library().nvfp4_linear_swiglu_gs(
+            x.data_ptr(), w_packed.data_ptr(), w_scale.data_ptr(), float(gate_global_scale),
+            float(up_global_scale), out.data_ptr(), M, N, K, int(flags),
+            ctypes.c_void_p(stream.cuda_stream))
+    if st != OK:
+        raise Nvfp4Error(st, "nvfp4_linear_swiglu_gs")
+    return out
 
 
 def choose_plan(M, N, K, flags=0):

@@ -118,6 +118,7 @@ struct Params {
   void* y;              // [M, N] (or [M, N/2] with swiglu), bf16 or f32
   int64_t M, N, K;
   float out_scale;      // 1 / global_scale
+  float out_scale_up;   // 1 / the up rows' global scale (SwiGLU)
   int stages_total;     // K / 256
   int split;            // CTAs per cluster along k
   int out_f32;          // 1: write f32 (before the bf16 rounding)
@@ -525,7 +526,7 @@ __global__ void __launch_bounds__(Roles<NM>::kThreads, NM == 16 ? 2 : 1)
         }
       }
       float yv = v * p.out_scale;
-      if (p.swiglu) yv = silu_mul(yv, u * p.out_scale);
+      if (p.swiglu) yv = silu_mul(yv, u * p.out_scale_up);
       const int64_t off = static_cast<int64_t>(m) * n_out + n_base + j;
       if (p.out_f32)
         static_cast<float*>(p.y)[off] = yv;

@@ -351,7 +351,7 @@ SmallmPlan plan_smallm(const DeviceInfo& d, int64_t M, int64_t N, int64_t K,
 
 template <int MT, bool F16>
 int launch_smallm(const DeviceInfo& d, const void* x, const uint8_t* wp, const uint8_t* ws,
-                  float gs, void* y, int64_t M, int64_t N, int64_t K, unsigned int flags,
+                  float gs, float gs_up, void* y, int64_t M, int64_t N, int64_t K, unsigned int flags,
                   cudaStream_t stream) {
   const bool swiglu = flags & NVFP4_FLAG_SWIGLU;
   const SmallmPlan plan = plan_smallm<MT, F16>(d, M, N, K, flags);
@@ -377,6 +377,7 @@ int launch_smallm(const DeviceInfo& d, const void* x, const uint8_t* wp, const u
   p.K = K;
   // f16 weights are exact code * scale; the bf16 ones carry 2^-10
   p.out_scale = F16 ? static_cast<float>(1.0 / static_cast<double>(gs)) : out_scale(gs);
+  p.out_scale_up = F16 ? static_cast<float>(1.0 / static_cast<double>(gs_up)) : out_scale(gs_up);
   p.stages_total = static_cast<int>(K / sm::kStageK);
   p.split = plan.split;
   p.lay = sm::make_layout(MT, plan.groups, plan.stages, F16, static_cast<int>(M));
@@ -468,7 +469,7 @@ GemvPlan plan_gemv(const DeviceInfo& d, int64_t M, int64_t N, int64_t K, unsigne
 
 template <int NM>
 int launch_gemv(const DeviceInfo& d, const void* x, const uint8_t* wp, const uint8_t* ws,
-                float gs, void* y, int64_t M, int64_t N, int64_t K, unsigned int flags,
+                float gs, float gs_up, void* y, int64_t M, int64_t N, int64_t K, unsigned int flags,
                 cudaStream_t stream) {
   const GemvPlan plan = plan_gemv<NM>(d, M, N, K, flags);
   if (plan.stages == 0) return NVFP4_ERR_INVALID;   // an override that cannot run
@@ -486,6 +487,7 @@ int launch_gemv(const DeviceInfo& d, const void* x, const uint8_t* wp, const uin
   p.N = N;
   p.K = K;
   p.out_scale = static_cast<float>(1.0 / static_cast<double>(gs));   // f16 weights are exact
+  p.out_scale_up = static_cast<float>(1.0 / static_cast<double>(gs_up));
   p.stages_total = static_cast<int>(K / gt::kStageK);
   p.split = plan.split;
   p.lay = gt::make_layout(NM, static_cast<int>(M), plan.stages);
@@ -516,7 +518,7 @@ int launch_gemv(const DeviceInfo& d, const void* x, const uint8_t* wp, const uin
 }
 
 int launch_tcgemm(const DeviceInfo& d, const void* x, const uint8_t* wp, const uint8_t* ws,
-                  float gs, void* y, int64_t M, int64_t N, int64_t K, unsigned int flags,
+                  float gs, float gs_up, void* y, int64_t M, int64_t N, int64_t K, unsigned int flags,
                   cudaStream_t stream) {
   namespace T = nvfp4::tcgemm;
   const bool swiglu = flags & NVFP4_FLAG_SWIGLU;
@@ -534,6 +536,7 @@ int launch_tcgemm(const DeviceInfo& d, const void* x, const uint8_t* wp, const u
   p.N = N;
   p.K = K;
   p.out_scale = out_scale(gs);
+  p.out_scale_up = out_scale(gs_up);
   p.out_f32 = (flags & NVFP4_FLAG_F32_OUT) ? 1 : 0;
   p.swiglu = swiglu ? 1 : 0;
   p.err = d.err;
@@ -562,8 +565,8 @@ int launch_tcgemm(const DeviceInfo& d, const void* x, const uint8_t* wp, const u
   return NVFP4_OK;
 }
 
-int run(const void* x, const uint8_t* wp, const uint8_t* ws, float gs, void* y, int64_t M,
-        int64_t N, int64_t K, unsigned int flags, void* stream_ptr) {
+int run(const void* x, const uint8_t* wp, const uint8_t* ws, float gs, float gs_up, void* y,
+        int64_t M, int64_t N, int64_t K, unsigned int flags, void* stream_ptr) {
   int st = validate(x, wp, ws, y, M, N, K, flags);
   if (st != NVFP4_OK) return st;
   if (M == 0) return NVFP4_OK;
@@ -573,21 +576,21 @@ int run(const void* x, const uint8_t* wp, const uint8_t* ws, float gs, void* y, 
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   const int kernel = kernel_for(M, flags);
   if (kernel == NVFP4_KERNEL_GEMV) {
-    if (M <= 16) return launch_gemv<16>(*d, x, wp, ws, gs, y, M, N, K, flags, stream);
-    return launch_gemv<32>(*d, x, wp, ws, gs, y, M, N, K, flags, stream);
+    if (M <= 16) return launch_gemv<16>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream);
+    return launch_gemv<32>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream);
   }
   if (kernel == NVFP4_KERNEL_SMALLM) {
     switch ((M + 7) / 8) {
       case 1:
         if (!(flags & NVFP4_FLAG_BF16_MMA))
-          return launch_smallm<1, true>(*d, x, wp, ws, gs, y, M, N, K, flags, stream);
-        return launch_smallm<1, false>(*d, x, wp, ws, gs, y, M, N, K, flags, stream);
-      case 2: return launch_smallm<2, false>(*d, x, wp, ws, gs, y, M, N, K, flags, stream);
-      case 3: return launch_smallm<3, false>(*d, x, wp, ws, gs, y, M, N, K, flags, stream);
-      default: return launch_smallm<4, false>(*d, x, wp, ws, gs, y, M, N, K, flags, stream);
+          return launch_smallm<1, true>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream);
+        return launch_smallm<1, false>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream);
+      case 2: return launch_smallm<2, false>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream);
+      case 3: return launch_smallm<3, false>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream);
+      default: return launch_smallm<4, false>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream);
     }
   }
-  return launch_tcgemm(*d, x, wp, ws, gs, y, M, N, K, flags, stream);
+  return launch_tcgemm(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream);
 }
 
 }  // namespace
@@ -610,32 +613,39 @@ const char* nvfp4_status_string(int status) {
 
 int nvfp4_linear(const void* x, const uint8_t* w_packed, const uint8_t* w_scale,
                  float global_scale, void* y, int64_t M, int64_t N, int64_t K, void* stream) {
-  return run(x, w_packed, w_scale, global_scale, y, M, N, K, 0u, stream);
+  return run(x, w_packed, w_scale, global_scale, global_scale, y, M, N, K, 0u, stream);
 }
 
 int nvfp4_linear_f32(const void* x, const uint8_t* w_packed, const uint8_t* w_scale,
                      float global_scale, float* y, int64_t M, int64_t N, int64_t K,
                      void* stream) {
-  return run(x, w_packed, w_scale, global_scale, y, M, N, K, NVFP4_FLAG_F32_OUT, stream);
+  return run(x, w_packed, w_scale, global_scale, global_scale, y, M, N, K, NVFP4_FLAG_F32_OUT, stream);
 }
 
 int nvfp4_linear_swiglu(const void* x, const uint8_t* w_packed, const uint8_t* w_scale,
                         float global_scale, void* y, int64_t M, int64_t N, int64_t K,
                         void* stream) {
-  return run(x, w_packed, w_scale, global_scale, y, M, N, K, NVFP4_FLAG_SWIGLU, stream);
+  return run(x, w_packed, w_scale, global_scale, global_scale, y, M, N, K, NVFP4_FLAG_SWIGLU, stream);
 }
 
 int nvfp4_linear_swiglu_f32(const void* x, const uint8_t* w_packed, const uint8_t* w_scale,
                             float global_scale, float* y, int64_t M, int64_t N, int64_t K,
                             void* stream) {
-  return run(x, w_packed, w_scale, global_scale, y, M, N, K,
+  return run(x, w_packed, w_scale, global_scale, global_scale, y, M, N, K,
              NVFP4_FLAG_SWIGLU | NVFP4_FLAG_F32_OUT, stream);
 }
 
 int nvfp4_linear_ex(const void* x, const uint8_t* w_packed, const uint8_t* w_scale,
                     float global_scale, void* y, int64_t M, int64_t N, int64_t K,
                     unsigned int flags, void* stream) {
-  return run(x, w_packed, w_scale, global_scale, y, M, N, K, flags, stream);
+  return run(x, w_packed, w_scale, global_scale, global_scale, y, M, N, K, flags, stream);
+}
+
+int nvfp4_linear_swiglu_gs(const void* x, const uint8_t* w_packed, const uint8_t* w_scale,
+                           float gate_global_scale, float up_global_scale, void* y, int64_t M,
+                           int64_t N, int64_t K, unsigned int flags, void* stream) {
+  return run(x, w_packed, w_scale, gate_global_scale, up_global_scale, y, M, N, K,
+             flags | NVFP4_FLAG_SWIGLU, stream);
 }
 
 int nvfp4_linear_kernel_for(int64_t M, int64_t N, int64_t K, unsigned int flags) {

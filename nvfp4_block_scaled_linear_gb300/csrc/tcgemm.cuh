@@ -67,6 +67,7 @@ struct Params {
   void* y;
   int64_t M, N, K;
   float out_scale;      // fp32(2^10 / global_scale)
+  float out_scale_up;   // the same for the up rows of SwiGLU (their own global scale)
   int out_f32;
   int swiglu;          // tile = 64 gate rows + the 64 matching up rows
   int tiles_w;         // weight tiles (N / 128)
@@ -312,6 +313,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t ncol = p.swiglu ? static_cast<int64_t>(bw) * 64 + (lane_row >> 1)
                                     : static_cast<int64_t>(bw) * kTileW + lane_row;
       const uint32_t t_acc = tmem_base + b * kAccCols + (static_cast<uint32_t>(32 * q) << 16);
+      // SwiGLU: odd A rows are up rows, with their own global scale
+      const float lane_scale = (p.swiglu && (lane & 1)) ? p.out_scale_up : p.out_scale;
 #pragma unroll 1
       for (int c0 = 0; c0 < kTileX; c0 += 32) {
         uint32_t v[32];
@@ -326,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           const int m = m_tile + c0 + j;
-          float yv = __uint_as_float(v[j]) * p.out_scale;
+          float yv = __uint_as_float(v[j]) * lane_scale;
           if (p.swiglu) {
             // lanes 2k (gate) and 2k+1 (up) share output column ncol; the
             // even lane takes the even activation rows, the odd lane the odd

@@ -100,6 +100,10 @@ def test_rejects_before_any_device_work(lib):
     assert _call(lib, A, A, A, A, 0, 256, 512) == 0
     assert _call(lib, None, A, A, None, 0, 256, 512) == 0
     assert _call(lib, None, None, A, None, 0, 256, 512) == -1
+    assert lib.nvfp4_linear_swiglu_gs(A, A, A, ctypes.c_float(1.0), ctypes.c_float(2.0), None,
+                                      1, 256, 512, 0, None) == -1
+    assert lib.nvfp4_linear_swiglu_gs(A, A, A, ctypes.c_float(1.0), ctypes.c_float(2.0), A,
+                                      1, 256, 384, 0, None) == -3
     # tuning overrides out of range
     assert lib.nvfp4_linear_ex(A, A, A, ctypes.c_float(1.0), A, 1, 256, 512,
                                _lib.FLAG_SPLIT(17), None) == -1

@@ -261,6 +261,34 @@ def test_non_finite_values_propagate(M, flags):
     assert np.all((ybf[np.isnan(y64)] & 0x7FFF) > 0x7F80)
 
 
+@pytest.mark.parametrize("M,kflag", [(1, 0), (7, _lib.FLAG_FORCE_SMALLM), (12, 0), (24, 0),
+                                     (7, _lib.FLAG_FORCE_GEMV), (64, 0), (300, 0)])
+def test_swiglu_separate_gate_up_global_scales(M, kflag):
+    """Gate rows with one global scale, up rows with another: equal to the
+    oracle's two half-linears combined by SwiGLU."""
+    N, K = 512, 1024
+    t = make_linear(M, N, K, seed=1800 + M)
+    gs_gate, gs_up = np.float32(448.0 / 6.0), np.float32(448.0 / 1.5)
+    H = N // 2
+    g64, ga = oracle.linear_f64(t.x_bits, t.w_packed[:H], t.w_scale[:H], gs_gate)
+    u64, ua = oracle.linear_f64(t.x_bits, t.w_packed[H:], t.w_scale[H:], gs_up)
+    y64 = np.concatenate([g64, u64], 1)
+    a = np.concatenate([ga, ua], 1)
+    out64 = oracle.swiglu_f64(y64)
+    x, wp, ws = to_dev(t)
+    y32 = _lib.linear_swiglu_gs(x, wp, ws, gs_gate, gs_up, kflag | _lib.FLAG_F32_OUT)
+    ybf = _lib.linear_swiglu_gs(x, wp, ws, gs_gate, gs_up, kflag)
+    torch.cuda.synchronize()
+    check_swiglu_f32(y32.cpu().numpy(), y64, a, out64, "swiglu_gs M=%d" % M)
+    check_swiglu_bf16(bf16_bits(ybf), y64, a, out64, oracle.to_bf16_bits(out64),
+                      "swiglu_gs M=%d" % M)
+    # equal scales: the same bits as the one-scale entry point
+    same = _lib.linear_swiglu_gs(x, wp, ws, t.global_scale, t.global_scale, kflag)
+    ref = _lib.linear_ex(x, wp, ws, float(t.global_scale), _lib.FLAG_SWIGLU | kflag)
+    torch.cuda.synchronize()
+    assert torch.equal(same.view(torch.int16), ref.view(torch.int16))
+
+
 # ------------------------------------------------------------------ exactness
 def _exhaustive_products():
     """Rows n = every e4m3 scale byte; inputs k = 0..15 carry codes 0..15;
