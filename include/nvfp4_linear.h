@@ -144,6 +144,21 @@ int nvfp4_linear_swiglu_gs(const void* x, const uint8_t* w_packed, const uint8_t
                            float gate_global_scale, float up_global_scale, void* y, int64_t M,
                            int64_t N, int64_t K, unsigned int flags, void* stream);
 
+/* One launch over a weight stacked from up to 8 projections that share
+ * their input, each with its own global scale -- e.g. a layer's q, k and v
+ * projections, quantised as separate checkpoint tensors (FlashRT docs,
+ * section 1, condition 3: q/k/v/o are NVFP4; one scale per tensor).
+ * w_packed / w_scale hold the segments' rows one after another
+ * (segment_rows[i] rows each, summing to N); y[M, N] holds their outputs
+ * side by side.  global_scales and segment_rows are host arrays of
+ * num_segments (1..8) entries.  `flags` as for nvfp4_linear_ex, without
+ * NVFP4_FLAG_SWIGLU.  Rejected (NVFP4_ERR_INVALID): a NULL array, a
+ * segment of no rows, rows not summing to N, or num_segments out of range. */
+int nvfp4_linear_segmented(const void* x, const uint8_t* w_packed, const uint8_t* w_scale,
+                           const float* global_scales, const int64_t* segment_rows,
+                           int num_segments, void* y, int64_t M, int64_t N, int64_t K,
+                           unsigned int flags, void* stream);
+
 /* General form of the four calls above; `flags` is an OR of NVFP4_FLAG_*.
  * The FORCE flags pick a kernel regardless of M (for A/B measurements and
  * for checking both kernels on the same inputs). */

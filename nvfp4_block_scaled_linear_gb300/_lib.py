@@ -82,6 +82,8 @@ def load_library(path=None):
     lib.nvfp4_linear_swiglu_gs.restype = ctypes.c_int
     lib.nvfp4_linear_swiglu_gs.argtypes = [P, P, P, ctypes.c_float, ctypes.c_float, P, i64, i64,
                                            i64, u32, P]
+    lib.nvfp4_linear_segmented.restype = ctypes.c_int
+    lib.nvfp4_linear_segmented.argtypes = [P, P, P, P, P, ctypes.c_int, P, i64, i64, i64, u32, P]
     lib.nvfp4_linear_kernel_for.restype = ctypes.c_int
     lib.nvfp4_linear_kernel_for.argtypes = [i64, i64, i64, u32]
     lib.nvfp4_device_status.restype = ctypes.c_int
@@ -206,6 +208,33 @@ def linear_swiglu_gs(x, w_packed, w_scale, gate_global_scale, up_global_scale, f
             ctypes.c_void_p(stream.cuda_stream))
     if st != OK:
         raise Nvfp4Error(st, "nvfp4_linear_swiglu_gs")
+    return out
+
+
+def linear_segmented(x, w_packed, w_scale, global_scales, segment_rows, flags=0, out=None,
+                     stream=None):
+    """nvfp4_linear_segmented: one launch over stacked projections, each row
+    segment with its own global scale; y holds the segments' outputs side by
+    side."""
+    w_packed, w_scale, M, N, K = _check(x, w_packed, w_scale)
+    gs = (ctypes.c_float * len(global_scales))(*[float(g) for g in global_scales])
+    rows = (ctypes.c_int64 * len(segment_rows))(*[int(r) for r in segment_rows])
+    dtype = torch.float32 if flags & FLAG_F32_OUT else torch.bfloat16
+    if out is None:
+        out = torch.empty((M, N), dtype=dtype, device=x.device)
+    elif (out.dtype != dtype or tuple(out.shape) != (M, N) or not out.is_contiguous()
+          or out.device != x.device):
+        raise ValueError("out must be a contiguous %s tensor of shape %s on %s"
+                         % (dtype, (M, N), x.device))
+    if stream is None:
+        stream = torch.cuda.current_stream(x.device)
+    with torch.cuda.device(x.device):
+        st = library().nvfp4_linear_segmented(
+            x.data_ptr(), w_packed.data_ptr(), w_scale.data_ptr(), ctypes.cast(gs, ctypes.c_void_p),
+            ctypes.cast(rows, ctypes.c_void_p), len(segment_rows), out.data_ptr(), M, N, K,
+            int(flags), ctypes.c_void_p(stream.cuda_stream))
+    if st != OK:
+        raise Nvfp4Error(st, "nvfp4_linear_segmented")
     return out
 
 

@@ -32,6 +32,25 @@ namespace nvfp4 {
 // epilogue, which multiplies the fp32 accumulator by fp32(2^10 / global_scale).
 constexpr float kWeightPow2 = 1024.0f;   // 2^10
 
+// Output-column segments with their own global scales (one launch over
+// weights stacked from several projections, e.g. q, k and v): output
+// column n < end[0] uses scale[0], n < end[1] scale[1], ...  n == 0: one
+// scale for all columns (the kernel's out_scale).
+constexpr int kMaxSegments = 8;
+struct SegScales {
+  int n;
+  int64_t end[kMaxSegments];
+  float scale[kMaxSegments];
+};
+
+__device__ __forceinline__ float seg_scale(const SegScales& s, int64_t col) {
+  float sc = s.scale[0];
+#pragma unroll
+  for (int i = 1; i < kMaxSegments; ++i)
+    if (i < s.n && col >= s.end[i - 1]) sc = s.scale[i];
+  return sc;
+}
+
 // SwiGLU epilogue: silu(g) * u = g / (1 + e^-g) * u, in fp32 with the CUDA
 // fast exponential and fast division (a few ulp; e^-g = inf gives 0).
 __device__ __forceinline__ float silu_mul(float g, float u) {

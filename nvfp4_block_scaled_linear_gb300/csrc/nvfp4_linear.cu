@@ -227,6 +227,27 @@ bool encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, ui
   return true;
 }
 
+// Host form of a segmented call: up to kMaxSegments row segments with their
+// global scales (count == 0: an ordinary call).
+struct SegSpec {
+  int count = 0;
+  int64_t end[nvfp4::kMaxSegments] = {};
+  float gs[nvfp4::kMaxSegments] = {};
+};
+
+// Fill a kernel's segment table, each scale in the kernel's units:
+// weight_pow2 / global_scale (2^10 for bf16 operands, 1 for f16).
+nvfp4::SegScales seg_table(const SegSpec* spec, double weight_pow2) {
+  nvfp4::SegScales t{};
+  if (!spec || spec->count == 0) return t;
+  t.n = spec->count;
+  for (int i = 0; i < spec->count; ++i) {
+    t.end[i] = spec->end[i];
+    t.scale[i] = static_cast<float>(weight_pow2 / static_cast<double>(spec->gs[i]));
+  }
+  return t;
+}
+
 // The global scale is applied as one fp32 multiply by 2^10 / global_scale
 // (2^10 undoes the exponent offset of the bf16 dequantised weights).
 float out_scale(float global_scale) {
@@ -352,7 +373,7 @@ SmallmPlan plan_smallm(const DeviceInfo& d, int64_t M, int64_t N, int64_t K,
 template <int MT, bool F16>
 int launch_smallm(const DeviceInfo& d, const void* x, const uint8_t* wp, const uint8_t* ws,
                   float gs, float gs_up, void* y, int64_t M, int64_t N, int64_t K, unsigned int flags,
-                  cudaStream_t stream) {
+                  cudaStream_t stream, const SegSpec* segs) {
   const bool swiglu = flags & NVFP4_FLAG_SWIGLU;
   const SmallmPlan plan = plan_smallm<MT, F16>(d, M, N, K, flags);
   if (plan.groups == 0) return NVFP4_ERR_INVALID;   // overrides that cannot run
@@ -378,6 +399,7 @@ int launch_smallm(const DeviceInfo& d, const void* x, const uint8_t* wp, const u
   // f16 weights are exact code * scale; the bf16 ones carry 2^-10
   p.out_scale = F16 ? static_cast<float>(1.0 / static_cast<double>(gs)) : out_scale(gs);
   p.out_scale_up = F16 ? static_cast<float>(1.0 / static_cast<double>(gs_up)) : out_scale(gs_up);
+  p.seg = seg_table(segs, F16 ? 1.0 : static_cast<double>(nvfp4::kWeightPow2));
   p.stages_total = static_cast<int>(K / sm::kStageK);
   p.split = plan.split;
   p.lay = sm::make_layout(MT, plan.groups, plan.stages, F16, static_cast<int>(M));
@@ -470,7 +492,7 @@ GemvPlan plan_gemv(const DeviceInfo& d, int64_t M, int64_t N, int64_t K, unsigne
 template <int NM>
 int launch_gemv(const DeviceInfo& d, const void* x, const uint8_t* wp, const uint8_t* ws,
                 float gs, float gs_up, void* y, int64_t M, int64_t N, int64_t K, unsigned int flags,
-                cudaStream_t stream) {
+                cudaStream_t stream, const SegSpec* segs) {
   const GemvPlan plan = plan_gemv<NM>(d, M, N, K, flags);
   if (plan.stages == 0) return NVFP4_ERR_INVALID;   // an override that cannot run
   CUtensorMap tw, ts, tx;
@@ -488,6 +510,7 @@ int launch_gemv(const DeviceInfo& d, const void* x, const uint8_t* wp, const uin
   p.K = K;
   p.out_scale = static_cast<float>(1.0 / static_cast<double>(gs));   // f16 weights are exact
   p.out_scale_up = static_cast<float>(1.0 / static_cast<double>(gs_up));
+  p.seg = seg_table(segs, 1.0);
   p.stages_total = static_cast<int>(K / gt::kStageK);
   p.split = plan.split;
   p.lay = gt::make_layout(NM, static_cast<int>(M), plan.stages);
@@ -519,7 +542,7 @@ int launch_gemv(const DeviceInfo& d, const void* x, const uint8_t* wp, const uin
 
 int launch_tcgemm(const DeviceInfo& d, const void* x, const uint8_t* wp, const uint8_t* ws,
                   float gs, float gs_up, void* y, int64_t M, int64_t N, int64_t K, unsigned int flags,
-                  cudaStream_t stream) {
+                  cudaStream_t stream, const SegSpec* segs) {
   namespace T = nvfp4::tcgemm;
   const bool swiglu = flags & NVFP4_FLAG_SWIGLU;
   CUtensorMap tx, tw, ts;
@@ -537,6 +560,7 @@ int launch_tcgemm(const DeviceInfo& d, const void* x, const uint8_t* wp, const u
   p.K = K;
   p.out_scale = out_scale(gs);
   p.out_scale_up = out_scale(gs_up);
+  p.seg = seg_table(segs, static_cast<double>(nvfp4::kWeightPow2));
   p.out_f32 = (flags & NVFP4_FLAG_F32_OUT) ? 1 : 0;
   p.swiglu = swiglu ? 1 : 0;
   p.err = d.err;
@@ -566,7 +590,8 @@ int launch_tcgemm(const DeviceInfo& d, const void* x, const uint8_t* wp, const u
 }
 
 int run(const void* x, const uint8_t* wp, const uint8_t* ws, float gs, float gs_up, void* y,
-        int64_t M, int64_t N, int64_t K, unsigned int flags, void* stream_ptr) {
+        int64_t M, int64_t N, int64_t K, unsigned int flags, void* stream_ptr,
+        const SegSpec* segs = nullptr) {
   int st = validate(x, wp, ws, y, M, N, K, flags);
   if (st != NVFP4_OK) return st;
   if (M == 0) return NVFP4_OK;
@@ -576,21 +601,21 @@ int run(const void* x, const uint8_t* wp, const uint8_t* ws, float gs, float gs_
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   const int kernel = kernel_for(M, flags);
   if (kernel == NVFP4_KERNEL_GEMV) {
-    if (M <= 16) return launch_gemv<16>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream);
-    return launch_gemv<32>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream);
+    if (M <= 16) return launch_gemv<16>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs);
+    return launch_gemv<32>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs);
   }
   if (kernel == NVFP4_KERNEL_SMALLM) {
     switch ((M + 7) / 8) {
       case 1:
         if (!(flags & NVFP4_FLAG_BF16_MMA))
-          return launch_smallm<1, true>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream);
-        return launch_smallm<1, false>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream);
-      case 2: return launch_smallm<2, false>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream);
-      case 3: return launch_smallm<3, false>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream);
-      default: return launch_smallm<4, false>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream);
+          return launch_smallm<1, true>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs);
+        return launch_smallm<1, false>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs);
+      case 2: return launch_smallm<2, false>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs);
+      case 3: return launch_smallm<3, false>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs);
+      default: return launch_smallm<4, false>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs);
     }
   }
-  return launch_tcgemm(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream);
+  return launch_tcgemm(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs);
 }
 
 }  // namespace
@@ -646,6 +671,27 @@ int nvfp4_linear_swiglu_gs(const void* x, const uint8_t* w_packed, const uint8_t
                            int64_t N, int64_t K, unsigned int flags, void* stream) {
   return run(x, w_packed, w_scale, gate_global_scale, up_global_scale, y, M, N, K,
              flags | NVFP4_FLAG_SWIGLU, stream);
+}
+
+int nvfp4_linear_segmented(const void* x, const uint8_t* w_packed, const uint8_t* w_scale,
+                           const float* global_scales, const int64_t* segment_rows,
+                           int num_segments, void* y, int64_t M, int64_t N, int64_t K,
+                           unsigned int flags, void* stream) {
+  if (!global_scales || !segment_rows || num_segments < 1 ||
+      num_segments > nvfp4::kMaxSegments || (flags & NVFP4_FLAG_SWIGLU))
+    return NVFP4_ERR_INVALID;
+  SegSpec spec;
+  spec.count = num_segments;
+  int64_t end = 0;
+  for (int i = 0; i < num_segments; ++i) {
+    if (segment_rows[i] <= 0) return NVFP4_ERR_INVALID;
+    end += segment_rows[i];
+    spec.end[i] = end;
+    spec.gs[i] = global_scales[i];
+  }
+  if (end != N) return NVFP4_ERR_INVALID;
+  return run(x, w_packed, w_scale, global_scales[0], global_scales[0], y, M, N, K, flags, stream,
+             &spec);
 }
 
 int nvfp4_linear_kernel_for(int64_t M, int64_t N, int64_t K, unsigned int flags) {

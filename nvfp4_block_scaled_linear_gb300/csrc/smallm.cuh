@@ -132,6 +132,7 @@ struct Params {
   int out_f32;          // 1: write f32 (before the bf16 rounding)
   int swiglu;           // 1: rows [0,N/2) gate, [N/2,N) up, y = silu(g)*u
   SmemLayout lay;
+  SegScales seg;        // per-segment scales (seg.n == 0: out_scale for every column)
   unsigned int* err;    // device error word
 };
 
@@ -521,7 +522,7 @@ __global__ void __launch_bounds__(threads_for(F16), F16 ? 2 : 1)
           if (p.swiglu) u += ld_cluster_f32(base + 4u * ((half_rows + j) * C + m));
         }
       }
-      float yv = v * p.out_scale;
+      float yv = v * (p.seg.n ? seg_scale(p.seg, n_base + j) : p.out_scale);
       if (p.swiglu) yv = silu_mul(yv, u * p.out_scale_up);
       const int64_t off = static_cast<int64_t>(m) * n_out + n_base + j;
       if (p.out_f32)

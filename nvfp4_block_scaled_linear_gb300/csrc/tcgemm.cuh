@@ -73,6 +73,7 @@ struct Params {
   int tiles_w;         // weight tiles (N / 128)
   int tiles_total;     // weight tiles x activation tiles
   int tiles_per_cta;   // consecutive tiles each CTA takes
+  SegScales seg;        // per-segment scales (seg.n == 0: out_scale for every column)
   unsigned int* err;
 };
 
@@ -314,7 +315,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     : static_cast<int64_t>(bw) * kTileW + lane_row;
       const uint32_t t_acc = tmem_base + b * kAccCols + (static_cast<uint32_t>(32 * q) << 16);
       // SwiGLU: odd A rows are up rows, with their own global scale
-      const float lane_scale = (p.swiglu && (lane & 1)) ? p.out_scale_up : p.out_scale;
+      const float lane_scale = p.seg.n ? seg_scale(p.seg, ncol)
+                               : ((p.swiglu && (lane & 1)) ? p.out_scale_up : p.out_scale);
 #pragma unroll 1
       for (int c0 = 0; c0 < kTileX; c0 += 32) {
         uint32_t v[32];

@@ -104,6 +104,21 @@ def test_rejects_before_any_device_work(lib):
                                       1, 256, 512, 0, None) == -1
     assert lib.nvfp4_linear_swiglu_gs(A, A, A, ctypes.c_float(1.0), ctypes.c_float(2.0), A,
                                       1, 256, 384, 0, None) == -3
+    gs2 = (ctypes.c_float * 2)(1.0, 2.0)
+    rows_ok = (ctypes.c_int64 * 2)(128, 128)
+    rows_bad = (ctypes.c_int64 * 2)(128, 64)
+    rows_zero = (ctypes.c_int64 * 2)(256, 0)
+    seg = lib.nvfp4_linear_segmented
+    assert seg(A, A, A, ctypes.cast(gs2, ctypes.c_void_p), ctypes.cast(rows_bad, ctypes.c_void_p),
+               2, A, 1, 256, 512, 0, None) == -1                       # rows sum != N
+    assert seg(A, A, A, ctypes.cast(gs2, ctypes.c_void_p), ctypes.cast(rows_zero, ctypes.c_void_p),
+               2, A, 1, 256, 512, 0, None) == -1                       # empty segment
+    assert seg(A, A, A, None, ctypes.cast(rows_ok, ctypes.c_void_p), 2, A, 1, 256, 512, 0,
+               None) == -1
+    assert seg(A, A, A, ctypes.cast(gs2, ctypes.c_void_p), ctypes.cast(rows_ok, ctypes.c_void_p),
+               9, A, 1, 256, 512, 0, None) == -1                       # > 8 segments
+    assert seg(A, A, A, ctypes.cast(gs2, ctypes.c_void_p), ctypes.cast(rows_ok, ctypes.c_void_p),
+               2, A, 1, 256, 512, _lib.FLAG_SWIGLU, None) == -1
     # tuning overrides out of range
     assert lib.nvfp4_linear_ex(A, A, A, ctypes.c_float(1.0), A, 1, 256, 512,
                                _lib.FLAG_SPLIT(17), None) == -1

@@ -289,6 +289,32 @@ def test_swiglu_separate_gate_up_global_scales(M, kflag):
     assert torch.equal(same.view(torch.int16), ref.view(torch.int16))
 
 
+@pytest.mark.parametrize("M,kflag", [(1, 0), (7, 0), (7, _lib.FLAG_FORCE_GEMV), (12, 0),
+                                     (32, 0), (100, 0)])
+def test_segmented_qkv_global_scales(M, kflag):
+    """q, k and v stacked into one launch, each with its own global scale:
+    equal to three separate oracle linears side by side (segments of 384,
+    128 and 128 rows: boundaries inside CTAs and tiles)."""
+    K = 1024
+    rows = [384, 128, 128]
+    gss = [np.float32(448.0 / 6.0), np.float32(448.0 / 2.0), np.float32(448.0 / 11.0)]
+    t = make_linear(M, sum(rows), K, seed=1900 + M)
+    ys, As = [], []
+    r0 = 0
+    for r, g in zip(rows, gss):
+        y64, a = oracle.linear_f64(t.x_bits, t.w_packed[r0:r0 + r], t.w_scale[r0:r0 + r], g)
+        ys.append(y64)
+        As.append(a)
+        r0 += r
+    y64, a = np.concatenate(ys, 1), np.concatenate(As, 1)
+    x, wp, ws = to_dev(t)
+    y32 = _lib.linear_segmented(x, wp, ws, gss, rows, kflag | _lib.FLAG_F32_OUT)
+    ybf = _lib.linear_segmented(x, wp, ws, gss, rows, kflag)
+    torch.cuda.synchronize()
+    check_f32(y32.cpu().numpy(), y64, a, "segmented M=%d" % M)
+    check_bf16(bf16_bits(ybf), y64, a, oracle.to_bf16_bits(y64), "segmented M=%d" % M)
+
+
 # ------------------------------------------------------------------ exactness
 def _exhaustive_products():
     """Rows n = every e4m3 scale byte; inputs k = 0..15 carry codes 0..15;
