@@ -57,6 +57,12 @@ def _load():
     lib.oracle_swiglu_rows.argtypes = [P, i64, i64, P]
     lib.oracle_decode_tables.restype = None
     lib.oracle_decode_tables.argtypes = [P, P]
+    lib.oracle_e4m3_round.restype = ctypes.c_uint
+    lib.oracle_e4m3_round.argtypes = [ctypes.c_float]
+    lib.oracle_e2m1_round.restype = ctypes.c_uint
+    lib.oracle_e2m1_round.argtypes = [ctypes.c_float]
+    lib.oracle_quantize.restype = ctypes.c_int
+    lib.oracle_quantize.argtypes = [P, i64, i64, P, P, P]
     _lib = lib
     return lib
 
@@ -163,3 +169,28 @@ def swiglu_f64(y64):
 
 def swiglu(gate: float, up: float) -> float:
     return _load().oracle_swiglu(float(gate), float(up))
+
+
+def e4m3_round(v):
+    """Nearest e4m3 code (bits) to a non-negative fp32 value (ties to even,
+    saturating at 448)."""
+    return int(_load().oracle_e4m3_round(float(v)))
+
+
+def e2m1_round(t):
+    """Nearest e2m1 code (sign | magnitude code) to an fp32 value (ties to
+    the even code, saturating at 6)."""
+    return int(_load().oracle_e2m1_round(float(t)))
+
+
+def quantize(w_bits):
+    """bf16 [N, K] (bits) -> (w_packed [N, K/2] u8, w_scale [N, K/16] u8,
+    global_scale fp32), per the quantiser reading in nvfp4_oracle.c."""
+    w_bits = np.ascontiguousarray(w_bits, np.uint16)
+    N, K = w_bits.shape
+    wp = np.zeros((N, K // 2), np.uint8)
+    ws = np.zeros((N, K // 16), np.uint8)
+    gs = np.zeros(1, np.float32)
+    if _load().oracle_quantize(_ptr(w_bits), N, K, _ptr(wp), _ptr(ws), _ptr(gs)) != 0:
+        raise ValueError("bad shape for the quantiser: %s" % (w_bits.shape,))
+    return wp, ws, np.float32(gs[0])

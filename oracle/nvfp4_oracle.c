@@ -263,3 +263,109 @@ void oracle_decode_tables(double* e2m1_16, double* e4m3_256)
     for (unsigned c = 0; c < 16; ++c) e2m1_16[c] = oracle_e2m1(c);
     for (unsigned b = 0; b < 256; ++b) e4m3_256[b] = oracle_e4m3(b);
 }
+
+/* ------------------------------------------------------------------------ */
+/* Quantiser: bf16 weights -> NVFP4 (codes, e4m3 block scales, fp32 global  */
+/* scale).                                                                   */
+/* ------------------------------------------------------------------------ */
+/*
+ * The pages fix the stored format (FlashRT docs, section 1, condition 2:
+ * weight_global_scale = 448 / amax; e4m3 block scales per 16 inputs; FP4
+ * e2m1 codes) and that dequantisation is code * block scale / global scale,
+ * but not the rounding steps.  Reading taken (the plainest one consistent
+ * with those facts), every step in fp32 with round-to-nearest-even:
+ *
+ *   amax = max |w| over the tensor;  gs = 448 / amax   (gs = 1 if amax = 0)
+ *   per 16-input block:  s = e4m3((amax_block * gs) / 6)   (saturating)
+ *   per weight:          code = e2m1((w * gs) / s)          (saturating;
+ *                        the sign kept, so a negative weight that rounds to
+ *                        zero gets the code -0; a block whose scale rounds
+ *                        to 0 gets all codes +0)
+ *
+ * so that code * s / gs reproduces w to within half an e2m1 step of the
+ * block.  The roundings are written as brute-force nearest searches over the
+ * formats' value tables (ties to the even code), not as bit tricks.
+ */
+
+/* Nearest e4m3 (E4M3FN) value to v >= 0, ties to the even code; values
+ * above the largest finite e4m3 (448) saturate to it; NaN gives the NaN
+ * pattern 0x7F. */
+static unsigned e4m3_round(float v)
+{
+    if (v != v) return 0x7Fu;
+    if (v >= 448.0f) return 0x7Eu;
+    unsigned best = 0;
+    double best_d = INFINITY;
+    for (unsigned b = 0; b <= 0x7Eu; ++b) {
+        const double d = fabs(oracle_e4m3(b) - (double)v);
+        if (d < best_d || (d == best_d && (b & 1u) == 0)) {
+            best = b;
+            best_d = d;
+        }
+    }
+    return best;
+}
+
+/* Nearest e2m1 magnitude code (0..7) to |t|, ties to the even code, values
+ * above 6 saturating to 6; the sign bit from t. */
+static unsigned e2m1_round(float t)
+{
+    const double a = fabs((double)t);
+    unsigned best = 0;
+    double best_d = INFINITY;
+    for (unsigned c = 0; c < 8u; ++c) {
+        const double d = fabs(oracle_e2m1(c) - a);
+        if (d < best_d || (d == best_d && (c & 1u) == 0)) {
+            best = c;
+            best_d = d;
+        }
+    }
+    return best | (signbit(t) ? 8u : 0u);   /* |t| > 6: nearest is 6 (saturation) */
+}
+
+/* Exposed for tests. */
+unsigned oracle_e4m3_round(float v) { return e4m3_round(v); }
+unsigned oracle_e2m1_round(float t) { return e2m1_round(t); }
+
+/* w_bits: bf16 [N][K] row-major, K % 16 == 0.  Outputs: w_packed [N][K/2]
+ * (low nibble = even k), w_scale [N][K/16] (e4m3 bits), *gs_out.  Returns 0,
+ * or -1 on a bad shape.  Non-finite weights are outside this reading. */
+int oracle_quantize(const uint16_t* w_bits, int64_t N, int64_t K, uint8_t* w_packed,
+                    uint8_t* w_scale, float* gs_out)
+{
+    if (N <= 0 || K <= 0 || K % 16) return -1;
+    float amax = 0.0f;
+    for (int64_t i = 0; i < N * K; ++i) {
+        const float a = fabsf((float)oracle_bf16_to_f64(w_bits[i]));
+        if (a > amax) amax = a;
+    }
+    const float gs = amax > 0.0f ? 448.0f / amax : 1.0f;
+    *gs_out = gs;
+    for (int64_t n = 0; n < N; ++n) {
+        for (int64_t b = 0; b < K / 16; ++b) {
+            const uint16_t* blk = w_bits + n * K + b * 16;
+            float amax_b = 0.0f;
+            for (int j = 0; j < 16; ++j) {
+                const float a = fabsf((float)oracle_bf16_to_f64(blk[j]));
+                if (a > amax_b) amax_b = a;
+            }
+            const float s_f = (amax_b * gs) / 6.0f;
+            const unsigned sbyte = e4m3_round(s_f);
+            w_scale[n * (K / 16) + b] = (uint8_t)sbyte;
+            const float s = (float)oracle_e4m3(sbyte);
+            for (int j = 0; j < 16; j += 2) {
+                unsigned c[2];
+                for (int h = 0; h < 2; ++h) {
+                    if (s == 0.0f) {
+                        c[h] = 0;
+                    } else {
+                        const float w = (float)oracle_bf16_to_f64(blk[j + h]);
+                        c[h] = e2m1_round((w * gs) / s);
+                    }
+                }
+                w_packed[n * (K / 2) + b * 8 + j / 2] = (uint8_t)(c[0] | (c[1] << 4));
+            }
+        }
+    }
+    return 0;
+}

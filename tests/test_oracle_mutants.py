@@ -36,6 +36,18 @@ MUTANTS = {
     "rne_ties_away": ("if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u)))",
                       "if (lower >= 0x8000u)"),
     "swiglu_no_sigmoid": ("return gate / (1.0 + exp(-gate)) * up;", "return gate * up;"),
+    "quant_block_divisor_4": ("const float s_f = (amax_b * gs) / 6.0f;",
+                              "const float s_f = (amax_b * gs) / 4.0f;"),
+    "quant_global_scale_inverted": ("const float gs = amax > 0.0f ? 448.0f / amax : 1.0f;",
+                                    "const float gs = amax > 0.0f ? amax / 448.0f : 1.0f;"),
+    "quant_e2m1_ties_odd": ("if (d < best_d || (d == best_d && (c & 1u) == 0)) {",
+                            "if (d < best_d || (d == best_d && (c & 1u) == 1)) {"),
+    "quant_e4m3_ties_odd": ("if (d < best_d || (d == best_d && (b & 1u) == 0)) {",
+                            "if (d < best_d || (d == best_d && (b & 1u) == 1)) {"),
+    "quant_codes_use_unrounded_scale": ("const float s = (float)oracle_e4m3(sbyte);",
+                                        "const float s = s_f;"),
+    "quant_nibbles_swapped": ("w_packed[n * (K / 2) + b * 8 + j / 2] = (uint8_t)(c[0] | (c[1] << 4));",
+                              "w_packed[n * (K / 2) + b * 8 + j / 2] = (uint8_t)(c[1] | (c[0] << 4));"),
 }
 
 
@@ -53,6 +65,12 @@ def _build(tmp_path, name, source):
     lib.oracle_f64_to_bf16_array.argtypes = [P, P, i64]
     lib.oracle_swiglu.restype = ctypes.c_double
     lib.oracle_swiglu.argtypes = [ctypes.c_double, ctypes.c_double]
+    lib.oracle_quantize.restype = ctypes.c_int
+    lib.oracle_quantize.argtypes = [P, i64, i64, P, P, P]
+    lib.oracle_e2m1_round.restype = ctypes.c_uint
+    lib.oracle_e2m1_round.argtypes = [ctypes.c_float]
+    lib.oracle_e4m3_round.restype = ctypes.c_uint
+    lib.oracle_e4m3_round.argtypes = [ctypes.c_float]
     return lib
 
 
@@ -96,6 +114,30 @@ def _pins_pass(lib) -> bool:
         return False
     if abs(lib.oracle_swiglu(1.0, 1.0) - 1.0 / (1.0 + np.exp(-1.0))) > 1e-15:
         return False
+    # quantiser: the e2m1 midpoint table, torch's e4m3 cast on ties, and the
+    # hand-worked blocks
+    for t, code in ((0.25, 0), (0.75, 2), (1.25, 2), (1.75, 4), (2.5, 4), (3.5, 6), (5.0, 6),
+                    (7.0, 7)):
+        if lib.oracle_e2m1_round(t) != code:
+            return False
+    ev = np.float32([9.5, 10.5, 0.0546875, 1.0 + 1.0 / 16, 448.0])
+    want = torch.from_numpy(ev).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    if [lib.oracle_e4m3_round(float(v)) for v in ev] != list(want):
+        return False
+    for case in json.load(open(os.path.join(GOLDEN, "quantize_blocks.json")))["cases"]:
+        w = torch.tensor(case["w"], dtype=torch.float32).to(torch.bfloat16) \
+            .view(torch.int16).numpy().view(np.uint16)
+        w = np.ascontiguousarray(w)
+        N, K = w.shape
+        wp = np.zeros((N, K // 2), np.uint8)
+        ws = np.zeros((N, K // 16), np.uint8)
+        gs = np.zeros(1, np.float32)
+        lib.oracle_quantize(_p(w), N, K, _p(wp), _p(ws), _p(gs))
+        codes = np.stack([wp & 0xF, wp >> 4], -1).reshape(N, K)
+        if (gs[0] != np.float32(case["global_scale"])
+                or not np.array_equal(ws, np.asarray(case["scale"], np.uint8))
+                or not np.array_equal(codes, np.asarray(case["codes"], np.uint8))):
+            return False
     return True
 
 
