@@ -370,6 +370,32 @@ def e2e_case(case, steps, stream, dev):
     return ms, h2d, d2h
 
 
+def quantize_case(lib, dev, stream, hbm_peak, N=34816, K=5120, steps=20):
+    """The load-time quantiser (bf16 -> NVFP4) on the decode projection's
+    weight shape: bytes = bf16 in + codes + scales out (HBM-bound)."""
+    import torch
+    g = torch.Generator(device="cpu").manual_seed(11)
+    w = (torch.randn((N, K), generator=g) * 0.02).to(torch.bfloat16).to(dev)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            lib.quantize(w, stream=stream)
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(steps):
+            lib.quantize(w, stream=stream)
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    nbytes = N * K * 2 + N * K // 2 + N * K // 16 + 4
+    gbs = nbytes / (ms / 1e3) / 1e9
+    del w
+    return {"ms_per_step": round(ms, 5), "kernel": "quantize", "shape": [N, K],
+            "GB/s": round(gbs, 1), "frac_hbm_peak": round(gbs / hbm_peak, 4)}
+
+
 def run_ours(args):
     import torch
     from nvfp4_block_scaled_linear_gb300 import build as cuda_build
@@ -461,6 +487,7 @@ def run_ours(args):
             e_tot, _ = time_case(head, min(args.steps, 500), 5, stream, world, None,
                                  graph=False)
             line["eager_ms_per_step"] = round(e_tot / min(args.steps, 500), 6)
+        extras["quantize"] = quantize_case(lib, dev, stream, hbm_peak)
         line["workloads"] = extras
         line["gpu_launches_extras"] = "not in the headline timed region"
     sampler.stop()

@@ -159,6 +159,23 @@ int nvfp4_linear_segmented(const void* x, const uint8_t* w_packed, const uint8_t
                            int num_segments, void* y, int64_t M, int64_t N, int64_t K,
                            unsigned int flags, void* stream);
 
+/* Quantise bf16 weights w[N, K] (device, row-major, 16-byte aligned,
+ * K % 16 == 0) into the format the calls above consume: w_packed[N, K/2]
+ * (device, 8-byte aligned), w_scale[N, K/16] and *global_scale (device
+ * fp32).  The pages (FlashRT docs, section 1, condition 2) fix the format and
+ * weight_global_scale = 448 / amax, not the rounding; the steps taken, in
+ * fp32 with round-to-nearest-even:
+ *   gs = 448 / max|w| (1 for an all-zero tensor);
+ *   block scale = e4m3((max|w in block| * gs) / 6), saturating at 448;
+ *   code = e2m1((w * gs) / block scale), saturating at 6, sign kept (a
+ *   negative weight that rounds to zero is -0); all codes +0 where the
+ *   block scale rounds to 0.
+ * Non-finite weights are outside this contract.  Asynchronous on `stream`
+ * (a memset and three kernels); *global_scale holds the tensor maximum
+ * until the last of them completes.  Allocates nothing. */
+int nvfp4_quantize(const void* w, int64_t N, int64_t K, uint8_t* w_packed, uint8_t* w_scale,
+                   float* global_scale, void* stream);
+
 /* General form of the four calls above; `flags` is an OR of NVFP4_FLAG_*.
  * The FORCE flags pick a kernel regardless of M (for A/B measurements and
  * for checking both kernels on the same inputs). */

@@ -84,6 +84,8 @@ def load_library(path=None):
                                            i64, u32, P]
     lib.nvfp4_linear_segmented.restype = ctypes.c_int
     lib.nvfp4_linear_segmented.argtypes = [P, P, P, P, P, ctypes.c_int, P, i64, i64, i64, u32, P]
+    lib.nvfp4_quantize.restype = ctypes.c_int
+    lib.nvfp4_quantize.argtypes = [P, i64, i64, P, P, P, P]
     lib.nvfp4_linear_kernel_for.restype = ctypes.c_int
     lib.nvfp4_linear_kernel_for.argtypes = [i64, i64, i64, u32]
     lib.nvfp4_device_status.restype = ctypes.c_int
@@ -236,6 +238,27 @@ def linear_segmented(x, w_packed, w_scale, global_scales, segment_rows, flags=0,
     if st != OK:
         raise Nvfp4Error(st, "nvfp4_linear_segmented")
     return out
+
+
+def quantize(w, stream=None):
+    """nvfp4_quantize: bf16 weights [N, K] -> (w_packed [N, K/2] u8,
+    w_scale [N, K/16] u8, global_scale [1] fp32), all on w's device."""
+    if not w.is_cuda:
+        raise ValueError("w must be a CUDA tensor")
+    if w.dtype != torch.bfloat16 or w.dim() != 2 or not w.is_contiguous():
+        raise TypeError("w must be a contiguous 2-D bfloat16 tensor")
+    N, K = w.shape
+    wp = torch.empty((N, K // 2), dtype=torch.uint8, device=w.device)
+    ws = torch.empty((N, K // 16), dtype=torch.uint8, device=w.device)
+    gs = torch.empty(1, dtype=torch.float32, device=w.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(w.device)
+    with torch.cuda.device(w.device):
+        st = library().nvfp4_quantize(w.data_ptr(), N, K, wp.data_ptr(), ws.data_ptr(),
+                                      gs.data_ptr(), ctypes.c_void_p(stream.cuda_stream))
+    if st != OK:
+        raise Nvfp4Error(st, "nvfp4_quantize")
+    return wp, ws, gs
 
 
 def choose_plan(M, N, K, flags=0):

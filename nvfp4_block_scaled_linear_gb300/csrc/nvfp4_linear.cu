@@ -12,6 +12,7 @@
 
 #include "../../include/nvfp4_linear.h"
 #include "gemv_tc.cuh"
+#include "quantize.cuh"
 #include "smallm.cuh"
 #include "tcgemm.cuh"
 
@@ -692,6 +693,40 @@ int nvfp4_linear_segmented(const void* x, const uint8_t* w_packed, const uint8_t
   if (end != N) return NVFP4_ERR_INVALID;
   return run(x, w_packed, w_scale, global_scales[0], global_scales[0], y, M, N, K, flags, stream,
              &spec);
+}
+
+int nvfp4_quantize(const void* w, int64_t N, int64_t K, uint8_t* w_packed, uint8_t* w_scale,
+                   float* global_scale, void* stream_ptr) {
+  namespace Q = nvfp4::quant;
+  if (!w || !w_packed || !w_scale || !global_scale || N <= 0 || K <= 0)
+    return NVFP4_ERR_INVALID;
+  if ((reinterpret_cast<uintptr_t>(w) & 15u) || (reinterpret_cast<uintptr_t>(w_packed) & 7u) ||
+      (reinterpret_cast<uintptr_t>(global_scale) & 3u))
+    return NVFP4_ERR_MISALIGNED;
+  if (K % 16 != 0 || N > (int64_t(1) << 31) || K > (int64_t(1) << 31)) return NVFP4_ERR_SHAPE;
+  DeviceInfo* d = nullptr;
+  const int st = device_setup(&d);
+  if (st != NVFP4_OK) return st;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  const int64_t n_blocks = N * (K / 16);
+  const int64_t grid_cap = static_cast<int64_t>(d->num_sms) * 8;
+  const unsigned g_amax = static_cast<unsigned>(
+      std::min<int64_t>(grid_cap, (2 * n_blocks + Q::kThreads - 1) / Q::kThreads));
+  const unsigned g_quant = static_cast<unsigned>(
+      std::min<int64_t>(grid_cap, (n_blocks + Q::kThreads - 1) / Q::kThreads));
+  unsigned int* amax_bits = reinterpret_cast<unsigned int*>(global_scale);
+  if (cudaMemsetAsync(global_scale, 0, sizeof(float), stream) != cudaSuccess) {
+    cudaGetLastError();
+    return NVFP4_ERR_LAUNCH;
+  }
+  Q::amax_kernel<<<g_amax, Q::kThreads, 0, stream>>>(static_cast<const uint4*>(w), 2 * n_blocks,
+                                                     amax_bits);
+  Q::quantize_kernel<<<g_quant, Q::kThreads, 0, stream>>>(
+      static_cast<const uint4*>(w), n_blocks, amax_bits, reinterpret_cast<uint2*>(w_packed),
+      w_scale);
+  Q::finalize_kernel<<<1, 32, 0, stream>>>(global_scale);
+  if (cudaGetLastError() != cudaSuccess) return NVFP4_ERR_LAUNCH;
+  return NVFP4_OK;
 }
 
 int nvfp4_linear_kernel_for(int64_t M, int64_t N, int64_t K, unsigned int flags) {

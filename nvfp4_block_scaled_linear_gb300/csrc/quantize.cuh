@@ -1,0 +1,125 @@
+// quantize.cuh -- bf16 weights -> the NVFP4 checkpoint format this library
+// consumes (FlashRT docs, "Qwen3.6-27B NVFP4 on RTX 5090", section 1,
+// condition 2: weight_packed FP4 e2m1 two per byte, weight_scale e4m3 per
+// 16 inputs, weight_global_scale = 448 / amax).
+//
+// The pages give the stored format and the dequantisation, not the rounding
+// steps; this follows the plainest reading consistent with them, every step
+// in fp32 with round-to-nearest-even:
+//   amax = max |w|;  gs = 448 / amax  (1 if amax = 0)
+//   per 16-input block:  s = e4m3((amax_block * gs) / 6), saturating
+//   per weight:          code = e2m1((w * gs) / s), saturating, sign kept;
+//                        all codes +0 where s rounds to 0
+// Both conversions are the hardware's (cvt.rn.satfinite.e4m3x2 / e2m1x2).
+//
+// Three stream-ordered steps, no workspace: the tensor maximum is gathered
+// by atomicMax into the caller's global-scale word (as fp32 bits: the bit
+// patterns of non-negative floats order like their values), the quantiser
+// reads it, and a last one-thread kernel turns it into 448 / amax.  The
+// quantiser streams its input once: HBM-bound.
+#pragma once
+#include <cstdint>
+#include <cuda_fp16.h>
+
+#include "ptx.cuh"
+
+namespace nvfp4 {
+namespace quant {
+
+constexpr int kThreads = 256;
+
+// |w| maximum over n_vec x 8 bf16 values, into *amax_bits (zeroed before).
+__global__ void __launch_bounds__(kThreads) amax_kernel(const uint4* __restrict__ w,
+                                                        int64_t n_vec,
+                                                        unsigned int* amax_bits) {
+  uint32_t m = 0;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(kThreads) + threadIdx.x; i < n_vec;
+       i += static_cast<int64_t>(gridDim.x) * kThreads) {
+    const uint4 v = w[i];
+    m = max_u16x2(m, max_u16x2(max_u16x2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
+                               max_u16x2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu)));
+  }
+  m = max(m & 0xFFFFu, m >> 16);
+  m = __reduce_max_sync(0xffffffffu, m);
+  __shared__ uint32_t red[kThreads / 32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) red[warp] = m;
+  __syncthreads();
+  if (warp == 0) {
+    m = lane < kThreads / 32 ? red[lane] : 0u;
+    m = __reduce_max_sync(0xffffffffu, m);
+    if (lane == 0 && m != 0) atomicMax(amax_bits, m << 16);   // bf16 -> fp32 bits
+  }
+}
+
+__device__ __forceinline__ float global_scale_of(float amax) {
+  return amax > 0.0f ? __fdiv_rn(448.0f, amax) : 1.0f;
+}
+
+// e4m3 bits of the nearest e4m3 to v (saturating), and their value.
+__device__ __forceinline__ uint32_t to_e4m3(float v) {
+  uint16_t d;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(0.0f), "f"(v));
+  return d & 0xFFu;
+}
+__device__ __forceinline__ float from_e4m3(uint32_t b) {
+  uint32_t h;
+  asm("{\n\t.reg .b16 s;\n\t"
+      "cvt.u16.u32 s, %1;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, s;\n\t}"
+      : "=r"(h)
+      : "r"(b));
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(h & 0xFFFFu)));
+}
+// Two codes in one byte: lo -> low nibble (even k), hi -> high nibble.
+__device__ __forceinline__ uint32_t to_e2m1x2(float lo, float hi) {
+  uint32_t d;
+  asm("{\n\t.reg .b8 b;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b, %1, %2;\n\t"
+      "cvt.u32.u8 %0, b;\n\t}"
+      : "=r"(d)
+      : "f"(hi), "f"(lo));
+  return d;
+}
+
+// One thread per 16-input block: n_blocks = N * K / 16 in row-major order.
+__global__ void __launch_bounds__(kThreads)
+    quantize_kernel(const uint4* __restrict__ w, int64_t n_blocks,
+                    const unsigned int* __restrict__ amax_bits, uint2* __restrict__ codes,
+                    uint8_t* __restrict__ scales) {
+  const float gs = global_scale_of(__uint_as_float(*amax_bits));
+  for (int64_t b = blockIdx.x * static_cast<int64_t>(kThreads) + threadIdx.x; b < n_blocks;
+       b += static_cast<int64_t>(gridDim.x) * kThreads) {
+    const uint4 v0 = w[2 * b], v1 = w[2 * b + 1];
+    const uint32_t words[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    float f[16];
+    float amax_b = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      f[2 * i] = __uint_as_float(words[i] << 16);
+      f[2 * i + 1] = __uint_as_float(words[i] & 0xFFFF0000u);
+      amax_b = fmaxf(amax_b, fmaxf(fabsf(f[2 * i]), fabsf(f[2 * i + 1])));
+    }
+    const uint32_t sbyte = to_e4m3(__fdiv_rn(__fmul_rn(amax_b, gs), 6.0f));
+    const float s = from_e4m3(sbyte);
+    uint32_t packed[2] = {0u, 0u};
+    if (s != 0.0f) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t byte = to_e2m1x2(__fdiv_rn(__fmul_rn(f[2 * i], gs), s),
+                                        __fdiv_rn(__fmul_rn(f[2 * i + 1], gs), s));
+        packed[i >> 2] |= byte << (8 * (i & 3));
+      }
+    }
+    codes[b] = make_uint2(packed[0], packed[1]);
+    scales[b] = static_cast<uint8_t>(sbyte);
+  }
+}
+
+// *gs = 448 / amax, in place over the gathered maximum.
+__global__ void finalize_kernel(float* gs) {
+  if (threadIdx.x == 0) *gs = global_scale_of(*gs);
+}
+
+}  // namespace quant
+}  // namespace nvfp4

@@ -119,6 +119,14 @@ def test_rejects_before_any_device_work(lib):
                9, A, 1, 256, 512, 0, None) == -1                       # > 8 segments
     assert seg(A, A, A, ctypes.cast(gs2, ctypes.c_void_p), ctypes.cast(rows_ok, ctypes.c_void_p),
                2, A, 1, 256, 512, _lib.FLAG_SWIGLU, None) == -1
+    q = lib.nvfp4_quantize
+    F = 0x20000            # fake 16-byte aligned float address, never dereferenced
+    assert q(None, 4, 64, A, A, F, None) == -1
+    assert q(A, 4, 64, A, A, None, None) == -1
+    assert q(A, 0, 64, A, A, F, None) == -1
+    assert q(A, 4, 40, A, A, F, None) == -3                  # K % 16
+    assert q(A + 8, 4, 64, A, A, F, None) == -2               # w not 16-byte aligned
+    assert q(A, 4, 64, A + 4, A, F, None) == -2               # codes not 8-byte aligned
     # tuning overrides out of range
     assert lib.nvfp4_linear_ex(A, A, A, ctypes.c_float(1.0), A, 1, 256, 512,
                                _lib.FLAG_SPLIT(17), None) == -1

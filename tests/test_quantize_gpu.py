@@ -1,0 +1,87 @@
+"""GPU parity of the quantiser (nvfp4_quantize) with the oracle's: codes,
+block scales and global scale bit for bit, on seeded weights shaped like a
+checkpoint's projections, with outlier rows, all-zero and tiny blocks (e4m3
+subnormal scales), weights that round to -0 and the saturation edge."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from nvfp4_block_scaled_linear_gb300 import _lib
+from nvfp4_block_scaled_linear_gb300 import build as cuda_build
+from nvfp4_block_scaled_linear_gb300.inputs import f32_to_bf16_bits
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda:0")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    cuda_build.build()
+    _lib.load_library()
+    _lib.device_error(clear=True)
+    yield
+    assert _lib.device_error(clear=True) == 0
+
+
+def _weights(N, K, seed):
+    rng = np.random.default_rng(seed)
+    w = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+    if N > 3:
+        w[1] *= 40.0                                   # an outlier row sets the tensor amax
+        w[2, : min(K, 64)] = 0.0                       # all-zero blocks
+        w[3] *= 1e-4                                   # tiny blocks: subnormal e4m3 scales
+    w[0, 5] = -1e-6                                    # rounds to -0 next to larger weights
+    return f32_to_bf16_bits(w)
+
+
+def _gpu(bits):
+    w = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(DEV)
+    wp, ws, gs = _lib.quantize(w)
+    torch.cuda.synchronize()
+    return wp.cpu().numpy(), ws.cpu().numpy(), np.float32(gs.cpu().numpy()[0])
+
+
+@pytest.mark.parametrize("N,K", [(1, 16), (7, 48), (64, 256), (300, 1024), (2048, 5120)])
+def test_quantize_bit_exact(N, K):
+    bits = _weights(N, K, seed=N * 3 + K)
+    wp, ws, gs = _gpu(bits)
+    wp_o, ws_o, gs_o = oracle.quantize(bits)
+    assert gs == gs_o
+    assert np.array_equal(ws, ws_o), np.argwhere(ws != ws_o)[:5]
+    assert np.array_equal(wp, wp_o), np.argwhere(wp != wp_o)[:5]
+
+
+def test_quantize_hand_values_and_saturation():
+    # one row: the tensor maximum 6 in block 0; block 1 crosses the e2m1
+    # midpoints of the oracle's table after scaling
+    w = np.zeros((2, 32), np.float32)
+    w[0, :8] = [6.0, 3.0, 1.5, -6.0, 0.5, 1.0, 2.0, 4.0]
+    w[1, 16:24] = [0.75, -0.375, 0.1875, 0.0625, 0.03125, -0.015625, 5.0, -5.9]
+    bits = f32_to_bf16_bits(w)
+    wp, ws, gs = _gpu(bits)
+    wp_o, ws_o, gs_o = oracle.quantize(bits)
+    assert gs == gs_o and np.array_equal(ws, ws_o) and np.array_equal(wp, wp_o)
+
+
+def test_all_zero_tensor():
+    bits = np.zeros((4, 64), np.uint16)
+    wp, ws, gs = _gpu(bits)
+    assert gs == np.float32(1.0) and not wp.any() and not ws.any()
+
+
+def test_quantised_weights_drive_the_linear():
+    """Quantise on the GPU, then run the linear on the result: equal to the
+    oracle's linear on the oracle's quantisation of the same weights."""
+    from _parity import check_f32
+    N, K, M = 512, 1024, 3
+    bits = _weights(N, K, seed=77)
+    w = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(DEV)
+    wp, ws, gs = _lib.quantize(w)
+    x_bits = f32_to_bf16_bits(np.random.default_rng(78).standard_normal((M, K)).astype(np.float32))
+    x = torch.from_numpy(x_bits.view(np.int16)).view(torch.bfloat16).to(DEV)
+    y = _lib.linear_f32(x, wp, ws, float(gs.item()))
+    torch.cuda.synchronize()
+    wp_o, ws_o, gs_o = oracle.quantize(bits)
+    y64, a = oracle.linear_f64(x_bits, wp_o, ws_o, gs_o)
+    check_f32(y.cpu().numpy(), y64, a, "quantise then linear")
