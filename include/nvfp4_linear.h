@@ -76,14 +76,18 @@ extern "C" {
 #define NVFP4_FLAG_SPLIT(n) (((unsigned int)(n) & 0x1Fu) << NVFP4_FLAG_SPLIT_SHIFT)
 /* Tuning override of the warp-MMA few-row kernel: CTAs of 16 * n weight
  * rows (1 <= n <= 8, at most 4 when M > 16) instead of the built-in
- * choice; n = 0 means automatic.  A combination that does not fit on the
- * device is rejected with NVFP4_ERR_INVALID. */
+ * choice; n = 0 means automatic.  For the bf16 tcgen05 few-row kernel it
+ * pins the lane groups instead (n = 2: two CTAs per SM, n = 4: one).  A
+ * combination that does not fit on the device is rejected with
+ * NVFP4_ERR_INVALID. */
 #define NVFP4_FLAG_GROUPS_SHIFT 13
 #define NVFP4_FLAG_GROUPS_MASK (0xFu << NVFP4_FLAG_GROUPS_SHIFT)
 #define NVFP4_FLAG_GROUPS(n) (((unsigned int)(n) & 0xFu) << NVFP4_FLAG_GROUPS_SHIFT)
-/* The warp-MMA few-row kernel multiplying in bf16, the activations as
- * given (exact for any activations; M <= 32).  Without it, both few-row
- * kernels multiply in f16: code * scale is exact in f16, and each
+/* Multiply in bf16, the activations as given (exact for any activations;
+ * M <= 32): the warp-MMA few-row kernel, or with NVFP4_FLAG_FORCE_GEMV the
+ * bf16 tcgen05 few-row kernel (which M = 17..32 uses by default on weight
+ * matrices of N * K >= 2^26).  Without it, the default few-row kernels for
+ * M <= 16 multiply in f16: code * scale is exact in f16, and each
  * activation row is brought to f16 after scaling by a power of two taken
  * from the row's maximum |x| (the warp-MMA kernel: running maximum; the
  * tcgen05 kernel: maximum within each 256-k stage), which is exact for
@@ -91,14 +95,16 @@ extern "C" {
  * rounds it like an f16 subnormal.  (The warp-MMA kernel uses f16 only for
  * M <= 8.) */
 #define NVFP4_FLAG_BF16_MMA (1u << 17)
-/* Force the tcgen05 few-row kernel (needs M <= 32; the default there). */
+/* Force the tcgen05 few-row kernel (needs M <= 32): in f16, or in bf16
+ * with NVFP4_FLAG_BF16_MMA. */
 #define NVFP4_FLAG_FORCE_GEMV (1u << 18)
 
 /* Kernel identifiers returned by nvfp4_linear_kernel_for. */
 #define NVFP4_KERNEL_NONE 0
 #define NVFP4_KERNEL_SMALLM 1       /* few rows, register-fed warp MMA (forced, or bf16) */
 #define NVFP4_KERNEL_TCGEMM 2       /* M > 32: tcgen05 / TMEM tensor-core GEMM */
-#define NVFP4_KERNEL_GEMV 3         /* M <= 32: weight streaming, dequantised into TMEM, tcgen05 */
+#define NVFP4_KERNEL_GEMV 3         /* M <= 32: weight streaming, dequantised into TMEM, tcgen05, f16 */
+#define NVFP4_KERNEL_GEMV_BF16 4    /* the same in bf16, accumulating in TMEM over all of k */
 
 /* Version of this ABI (NVFP4_ABI_VERSION). */
 int nvfp4_abi_version(void);

@@ -33,8 +33,9 @@ def FLAG_GROUPS(n):
     return (int(n) & 0xF) << 13
 
 
-KERNEL_NONE, KERNEL_SMALLM, KERNEL_TCGEMM, KERNEL_GEMV = 0, 1, 2, 3
-KERNEL_NAMES = {KERNEL_SMALLM: "smallm", KERNEL_TCGEMM: "tcgemm", KERNEL_GEMV: "gemv_tc"}
+KERNEL_NONE, KERNEL_SMALLM, KERNEL_TCGEMM, KERNEL_GEMV, KERNEL_GEMV_BF16 = 0, 1, 2, 3, 4
+KERNEL_NAMES = {KERNEL_SMALLM: "smallm", KERNEL_TCGEMM: "tcgemm", KERNEL_GEMV: "gemv_tc",
+                KERNEL_GEMV_BF16: "gemv_bf16"}
 
 HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
                       "include", "nvfp4_linear.h")

@@ -1,0 +1,428 @@
+// gemv_bf16.cuh -- NVFP4 W4A16 linear for few activation rows (M <= 32) on
+// the tcgen05 tensor cores, in bf16: decode (M = 1), speculative verify
+// (M = K+1, FlashRT docs section 3) and small continuous batches.
+//
+// The layer is bound by streaming the packed weights and scales from HBM
+// once.  The CUDA cores dequantise, the tensor core does every multiply-add,
+// and nothing in the main loop depends on reading results back:
+//
+//  * One CTA owns 128 weight rows (the MMA's M; SwiGLU: 64 gate rows and
+//    the 64 matching up rows) and a contiguous range of k.  A producer warp
+//    streams 256-k stages -- packed codes (128B-swizzled), block scales and
+//    the activations -- into a shared-memory ring with TMA.  The activation
+//    tile is the MMA's B operand as it lands: bf16, 128B-swizzled K-major,
+//    NM = 16 or 32 rows, the rows past M filled with zeros by the copy.
+//  * A stage is four 64-k jobs.  Job j goes to lane group j mod NI: four
+//    dequantisation warps (one per 32-row TMEM lane quadrant) write the
+//    job's weights as bf16 code * scale * 2^-10 (exact) into that group's
+//    TMEM ring, and the group's own MMA issuer adds A (TMEM) x B (shared
+//    memory) into the group's own fp32 accumulator in TMEM.  NI issuers run
+//    side by side: one thread issues at most one tcgen05.mma every
+//    ~30-60 ns, far below what the tensor core accepts from several.
+//  * The accumulators stay in TMEM for the whole k range; the epilogue reads
+//    them once, sums the NI groups and applies 2^10 / global scale.
+//  * Split-K: CTAs that share rows but not k form one thread-block cluster;
+//    partials are reduced across the cluster through distributed shared
+//    memory.  No global workspace, no atomics, no waits on other CTAs.
+#pragma once
+#include <cstdint>
+#include <cuda_bf16.h>
+
+#include "dequant.cuh"
+#include "ptx.cuh"
+
+namespace nvfp4 {
+namespace gemvbf {
+
+constexpr int kRows = 128;              // weight rows per CTA (the MMA's M)
+constexpr int kHalfRows = kRows / 2;    // one TMA box of rows
+constexpr int kStageK = 256;            // k per pipeline stage
+constexpr int kJobK = 64;               // k per job (one TMEM slot, 32 columns)
+constexpr int kJobsPerStage = kStageK / kJobK;
+constexpr int kSlotCols = kJobK / 2;    // bf16 pairs per TMEM column
+constexpr int kSlotsPerGroup = 3;       // TMEM weight ring depth of one lane group
+constexpr int kMaxSplit = 16;           // cluster size limit (non-portable above 8)
+
+// Warp roles for NI lane groups: warp 0 the producer, warps 1..NI the
+// issuers, then NI quartets of dequantisation warps.  NI = 4 runs one CTA
+// per SM (TMEM 512 columns), NI = 2 two CTAs per SM (256 columns each).
+template <int NM, int NI>
+struct Roles {
+  static constexpr int kWarpProducer = 0;
+  static constexpr int kWarpMma = 1;
+  static constexpr int kWarpDeq = 1 + NI;
+  static constexpr int kDeqWarps = 4 * NI;
+  static constexpr int kThreads = (kWarpDeq + kDeqWarps) * 32;
+  static constexpr int kCtasPerSm = NI == 4 ? 1 : 2;
+  static constexpr int kDCol = NI * kSlotsPerGroup * kSlotCols;   // accumulators' first column
+  static constexpr uint32_t kTmemCols = 512 / kCtasPerSm;
+  static_assert(NI == 2 || NI == 4, "two or four lane groups");
+  static_assert(kDCol + NI * NM <= static_cast<int>(kTmemCols), "TMEM plan");
+};
+
+__host__ __device__ constexpr int align_up(int v, int a) { return (v + a - 1) / a * a; }
+
+// Shared-memory layout of one launch (byte offsets from the 1024-aligned
+// base), computed on the host per call.  A stage holds the codes
+// [128 rows][128 B] (128B-swizzled), the scales [128 rows][16 B] and the
+// activations: four 64-k column blocks of [NM rows][128 B], 128B-swizzled.
+struct SmemLayout {
+  int stages;
+  int stage_bytes;
+  int s_off;        // scales, within a stage
+  int x_off;        // activations, within a stage
+  int lut_off;      // 256 bf16 scale pairs
+  int bar_off;      // mbarriers, abort flag, TMEM base
+  int total;        // dynamic shared memory to request (with alignment slack)
+};
+
+__host__ __device__ constexpr int num_barriers(int stages, int ni) {
+  return 2 * stages + ni * kSlotsPerGroup + 1;
+}
+
+__host__ __device__ constexpr SmemLayout make_layout(int nm, int ni, int stages) {
+  SmemLayout l{};
+  l.stages = stages;
+  l.s_off = kRows * 128;
+  l.x_off = align_up(l.s_off + kRows * 16, 1024);
+  l.stage_bytes = align_up(l.x_off + nm * kStageK * 2, 1024);
+  l.lut_off = stages * l.stage_bytes;
+  l.bar_off = l.lut_off + 256 * 4;
+  l.total = l.bar_off + num_barriers(stages, ni) * 8 + 16 + 1024;
+  return l;
+}
+
+// A dequantisation warp waits for the stage of its job kSlotsPerGroup jobs
+// back on that stage's `empty` barrier; for the parity to be unambiguous the
+// barrier must not have moved on by two phases, which holds while a lane
+// group's ring is shallower than the jobs it sees in stages - 1 stages.  The
+// final exchange reuses the ring; it must fit.
+__host__ __device__ constexpr bool layout_ok(const SmemLayout& l, int nm, int ni) {
+  return l.stages >= 2 && kSlotsPerGroup * ni <= kJobsPerStage * (l.stages - 1) &&
+         kRows * nm * 4 <= l.stages * l.stage_bytes;
+}
+
+struct Params {
+  void* y;              // [M, N] (or [M, N/2] with swiglu), bf16 or f32
+  int64_t M, N, K;
+  float out_scale;      // fp32(2^10 / global_scale)
+  float out_scale_up;   // the same for the up rows of SwiGLU (their own global scale)
+  int stages_total;     // K / 256
+  int split;            // CTAs per cluster along k
+  int out_f32;          // 1: write f32 (before the bf16 rounding)
+  int swiglu;           // 1: rows [0,N/2) gate, [N/2,N) up, y = silu(g)*u
+  SmemLayout lay;
+  SegScales seg;        // per-segment scales (seg.n == 0: out_scale for every column)
+  unsigned int* err;    // device error word
+};
+
+// A wait whose outcome the whole warp shares: the warp-aligned tcgen05
+// instructions after it need every lane converged.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity,
+                                          volatile int* abort_flag) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag));
+}
+
+template <int NM, int NI>
+__global__ void __launch_bounds__(Roles<NM, NI>::kThreads, Roles<NM, NI>::kCtasPerSm)
+    gemv_bf16_kernel(const __grid_constant__ CUtensorMap tm_w,
+                     const __grid_constant__ CUtensorMap tm_s,
+                     const __grid_constant__ CUtensorMap tm_x, const Params p) {
+  static_assert(NM == 16 || NM == 32, "MMA N is 16 or 32");
+  using R = Roles<NM, NI>;
+  constexpr int kThreads = R::kThreads;
+  const SmemLayout& L = p.lay;
+  const int S = L.stages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint32_t* lut = reinterpret_cast<uint32_t*>(smem + L.lut_off);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bar_off);   // TMA landed
+  // Stage consumed: every issuer has committed its last job of the stage
+  // (one tcgen05.commit per stage and issuer).  It releases the ring slot to
+  // the producer and the stage's TMEM weight slots to the dequantisers.
+  uint64_t* empty = full + S;
+  uint64_t* a_full = empty + S;                  // [NI][3] TMEM weights written
+  uint64_t* mma_done = a_full + NI * kSlotsPerGroup;   // every MMA has completed
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(mma_done + 1);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1) + 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int M = static_cast<int>(p.M);
+  const int split = p.split;
+  const int z = blockIdx.y;                                  // k-slice index
+  const int st_begin = static_cast<int>((int64_t)p.stages_total * z / split);
+  const int st_end = static_cast<int>((int64_t)p.stages_total * (z + 1) / split);
+  const int n_stages = st_end - st_begin;
+  // jobs of lane group i: i, i + NI, ... < 4 * n_stages
+  const int n_jobs_total = kJobsPerStage * n_stages;
+
+  // Weight rows of this CTA, as two boxes of 64 rows: consecutive rows, or
+  // (SwiGLU) 64 gate rows and the 64 matching up rows.
+  int row0, row1;
+  if (p.swiglu) {
+    row0 = blockIdx.x * kHalfRows;
+    row1 = static_cast<int>(p.N / 2) + blockIdx.x * kHalfRows;
+  } else {
+    row0 = blockIdx.x * kRows;
+    row1 = row0 + kHalfRows;
+  }
+
+  for (int i = threadIdx.x; i < 256; i += kThreads) lut[i] = scale_pair_from_e4m3(i);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], NI);
+    }
+    for (int a = 0; a < NI * kSlotsPerGroup; ++a) mbar_init(&a_full[a], 4);
+    mbar_init(mma_done, NI);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == R::kWarpMma) {
+    tmem_alloc(tmem_slot, R::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  // Let the next kernel in the stream launch now: its CTAs take the SM room
+  // this grid leaves free and prefetch their weights while this one runs.
+  // (They read this kernel's results only after griddepcontrol.wait, which
+  // waits for the whole grid to complete.)
+  if (threadIdx.x == 0) griddep_launch_dependents();
+
+  if (warp == R::kWarpProducer) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tensormap(&tm_w);
+      prefetch_tensormap(&tm_s);
+      prefetch_tensormap(&tm_x);
+      const uint64_t pol_stream = policy_evict_first();
+      const uint64_t pol_keep = policy_evict_last();
+      const uint32_t tx =
+          static_cast<uint32_t>(kRows * (kStageK / 2 + kStageK / 16) + NM * kStageK * 2);
+      auto issue_weights = [&](int it, int slot) {
+        uint8_t* st = smem + slot * L.stage_bytes;
+        const int k0 = (st_begin + it) * kStageK;
+        tma_load_2d_hint(st, &tm_w, &full[slot], k0 / 2, row0, pol_stream);
+        tma_load_2d_hint(st + kHalfRows * 128, &tm_w, &full[slot], k0 / 2, row1, pol_stream);
+        tma_load_2d_hint(st + L.s_off, &tm_s, &full[slot], k0 / 16, row0, pol_stream);
+        tma_load_2d_hint(st + L.s_off + kHalfRows * 16, &tm_s, &full[slot], k0 / 16, row1,
+                         pol_stream);
+      };
+      auto issue_acts = [&](int it, int slot) {
+        uint8_t* st = smem + slot * L.stage_bytes;
+        const int k0 = (st_begin + it) * kStageK;
+#pragma unroll
+        for (int q = 0; q < kJobsPerStage; ++q)
+          tma_load_2d_hint(st + L.x_off + q * (NM * 128), &tm_x, &full[slot], k0 + kJobK * q, 0,
+                           pol_keep);
+      };
+      // The weights do not depend on the preceding kernel in the stream:
+      // fill the ring with them first, then wait for that kernel before
+      // touching the activations.
+      const int pre = n_stages < S ? n_stages : S;
+      for (int it = 0; it < pre; ++it) {
+        mbar_arrive_expect_tx(&full[it], tx);
+        issue_weights(it, it);
+      }
+      griddep_wait();
+      for (int it = 0; it < pre; ++it) issue_acts(it, it);
+      int issued = pre;
+      int slot = pre == S ? 0 : pre;
+      uint32_t par = pre == S ? 0u : 1u;
+      for (int it = pre; it < n_stages; ++it) {
+        if (!mbar_wait(&empty[slot], par, abort_flag)) break;
+        mbar_arrive_expect_tx(&full[slot], tx);
+        issue_weights(it, slot);
+        issue_acts(it, slot);
+        ++issued;
+        if (++slot == S) {
+          slot = 0;
+          par ^= 1u;
+        }
+      }
+      // Drain: never leave a copy in flight into this CTA's shared memory.
+      const int first = issued > S ? issued - S : 0;
+      for (int it = first; it < issued; ++it) {
+        volatile int no_abort = 0;
+        if (!mbar_wait(&full[it % S], (it / S) & 1, &no_abort)) atomicOr(p.err, kErrWaitTimeout);
+      }
+    }
+  } else if (warp < R::kWarpDeq) {
+    // ------------------------------------------------------------ MMA issue
+    // Issuer i takes jobs i, i + NI, ...: job j is k [64 (j % 4), +64) of
+    // stage j / 4, four MMAs of K = 16 into accumulator i.  It commits once
+    // per stage, after its last job there.
+    const int gi = warp - R::kWarpMma;
+    if (lane == 0) {
+      constexpr uint32_t idesc = umma_idesc_bf16(kRows, NM);
+      const uint32_t d_tmem = tmem + R::kDCol + gi * NM;
+      int n = 0, aslot = 0;
+      uint32_t apar = 0;
+      for (int j = gi; j < n_jobs_total; j += NI, ++n) {
+        const int s = j / kJobsPerStage, q = j % kJobsPerStage;
+        const int slot = s % S;
+        if (!mbar_wait(&full[slot], static_cast<uint32_t>(s / S) & 1u, abort_flag)) break;
+        if (!mbar_wait(&a_full[gi * kSlotsPerGroup + aslot], apar, abort_flag)) break;
+        tc_fence_after_sync();
+        const uint64_t b_desc0 =
+            umma_desc_sw128(smem_addr(smem + slot * L.stage_bytes + L.x_off + q * (NM * 128)));
+        const uint32_t a_tmem = tmem + (gi * kSlotsPerGroup + aslot) * kSlotCols;
+#pragma unroll
+        for (int kk = 0; kk < kJobK / 16; ++kk)
+          umma_f16_tmem_a(d_tmem, a_tmem + kk * 8, b_desc0 + static_cast<uint64_t>((kk * 32) >> 4),
+                          idesc, (n > 0 || kk > 0) ? 1u : 0u);
+        if (q + NI >= kJobsPerStage) umma_commit(&empty[slot]);
+        if (++aslot == kSlotsPerGroup) {
+          aslot = 0;
+          apar ^= 1u;
+        }
+      }
+      // The accumulators are final once every MMA issued has completed.
+      umma_commit(mma_done);
+    }
+  } else {
+    // ------------------------------------------------------------ dequantisers
+    // Warp (lane group gi, quadrant qd): lane = weight row 32 qd + lane = its
+    // TMEM lane; for each job of the group it writes the row's 64 k as 32
+    // bf16 pairs (k 2c, 2c+1 in column c) into the group's next TMEM slot.
+    const int dw = warp - R::kWarpDeq;
+    const int gi = dw >> 2, qd = warp & 3;
+    const int row = 32 * qd + lane;
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(32 * qd) << 16);
+    int n = 0, aslot = 0;
+    for (int j = gi; j < n_jobs_total; j += NI, ++n) {
+      const int s = j / kJobsPerStage, q = j % kJobsPerStage;
+      const int slot = s % S;
+      if (!warp_wait(&full[slot], static_cast<uint32_t>(s / S) & 1u, abort_flag)) break;
+      if (n >= kSlotsPerGroup) {
+        // the slot's previous job (kSlotsPerGroup jobs back) must be done
+        const int s_prev = (j - NI * kSlotsPerGroup) / kJobsPerStage;
+        if (!warp_wait(&empty[s_prev % S], static_cast<uint32_t>(s_prev / S) & 1u, abort_flag))
+          break;
+      }
+      const uint8_t* st = smem + slot * L.stage_bytes;
+      // 64 k = code chunks 2q, 2q+1 of the row's 128-byte swizzled line
+      const uint4 w0 =
+          *reinterpret_cast<const uint4*>(st + row * 128 + (((2 * q) ^ (row & 7)) << 4));
+      const uint4 w1 =
+          *reinterpret_cast<const uint4*>(st + row * 128 + (((2 * q + 1) ^ (row & 7)) << 4));
+      // scales of the four 16-k blocks: bytes 4q .. 4q+3 of the row
+      const uint32_t s4 = *reinterpret_cast<const uint32_t*>(st + L.s_off + row * 16 + 4 * q);
+      const uint32_t S0 = lut[s4 & 0xFFu], S1 = lut[(s4 >> 8) & 0xFFu];
+      const uint32_t S2 = lut[(s4 >> 16) & 0xFFu], S3 = lut[s4 >> 24];
+      const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+      const uint32_t sc[4] = {S0, S1, S2, S3};
+      uint32_t out[32];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        uint32_t t[4];
+        dequant8_strided(words[i], sc[i >> 1], t);
+        pair_consecutive(t, &out[4 * i]);
+      }
+      tc_fence_after_sync();
+      tmem_st_32cols(t_lane + (gi * kSlotsPerGroup + aslot) * kSlotCols, out);
+      tmem_st_wait();
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&a_full[gi * kSlotsPerGroup + aslot]);
+      if (++aslot == kSlotsPerGroup) aslot = 0;
+    }
+  }
+
+  // ---------------------------------------------------------------- accumulators
+  // The first quartet reads the NI accumulators (lane = weight row) once
+  // every MMA has completed, and leaves their sum in the ring as the CTA's
+  // partial [128 rows][NM].
+  {
+    volatile int no_abort = 0;
+    const bool first_quartet = warp >= R::kWarpDeq && warp < R::kWarpDeq + 4;
+    bool ok = true;
+    if (first_quartet) ok = warp_wait(mma_done, 0, &no_abort);
+    if (first_quartet && !ok && lane == 0) atomicOr(p.err, kErrWaitTimeout);
+    tc_fence_before_sync();
+    __syncthreads();            // every role is done with the ring
+    if (first_quartet && ok) {
+      tc_fence_after_sync();
+      const int qd = warp & 3;
+      const uint32_t t_lane = tmem + (static_cast<uint32_t>(32 * qd) << 16) + R::kDCol;
+      float* part = reinterpret_cast<float*>(smem);
+      const int row = 32 * qd + lane;
+#pragma unroll
+      for (int h = 0; h < NM / 16; ++h) {
+        float sum[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) sum[c] = 0.f;
+#pragma unroll
+        for (int gi = 0; gi < NI; ++gi) {
+          uint32_t d[16];
+          tmem_ld_16cols(t_lane + gi * NM + 16 * h, d);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 16; ++c) sum[c] += __uint_as_float(d[c]);
+        }
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+          if (16 * h + c < M) part[row * NM + 16 * h + c] = sum[c];
+      }
+    }
+  }
+  if (*abort_flag && threadIdx.x == 0) atomicOr(p.err, kErrWaitTimeout);
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == R::kWarpMma) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, R::kTmemCols);
+  }
+  float* part = reinterpret_cast<float*>(smem);
+
+  // ---------------------------------------------------------------- epilogue
+  // Every CTA of the cluster finishes its partial; CTA z then reduces a
+  // 1/split share of the outputs across the cluster's shared memories.
+  // (Reconverge each warp first: the cluster barrier is a warp-aligned op.)
+  __syncwarp();
+  if (split > 1)
+    cluster_sync();
+  else
+    __syncthreads();
+  {
+    const int Rn = p.swiglu ? kHalfRows : kRows;           // outputs per activation row
+    const int items = Rn * M;
+    const int i0 = static_cast<int>((int64_t)items * z / split);
+    const int i1 = static_cast<int>((int64_t)items * (z + 1) / split);
+    const uint32_t part_local = smem_addr(part);
+    const int64_t n_out = p.swiglu ? p.N / 2 : p.N;
+    const int64_t n_base = static_cast<int64_t>(blockIdx.x) * Rn;
+    for (int i = i0 + threadIdx.x; i < i1; i += kThreads) {
+      const int m = i / Rn, jr = i % Rn;
+      float v = 0.f, u = 0.f;
+      if (split == 1) {
+        v = part[jr * NM + m];
+        if (p.swiglu) u = part[(kHalfRows + jr) * NM + m];
+      } else {
+        for (int c = 0; c < split; ++c) {
+          const uint32_t base = map_to_rank(part_local, c);
+          v += ld_cluster_f32(base + 4u * (jr * NM + m));
+          if (p.swiglu) u += ld_cluster_f32(base + 4u * ((kHalfRows + jr) * NM + m));
+        }
+      }
+      float yv = v * (p.seg.n ? seg_scale(p.seg, n_base + jr) : p.out_scale);
+      if (p.swiglu) yv = silu_mul(yv, u * p.out_scale_up);
+      const int64_t off = static_cast<int64_t>(m) * n_out + n_base + jr;
+      if (p.out_f32)
+        static_cast<float*>(p.y)[off] = yv;
+      else
+        static_cast<__nv_bfloat16*>(p.y)[off] = __float2bfloat16_rn(yv);
+    }
+  }
+  if (split > 1) {
+    __syncwarp();
+    cluster_sync();   // keep every partial alive until all readers are done
+  }
+}
+
+}  // namespace gemvbf
+}  // namespace nvfp4

@@ -11,6 +11,7 @@
 #include <mutex>
 
 #include "../../include/nvfp4_linear.h"
+#include "gemv_bf16.cuh"
 #include "gemv_tc.cuh"
 #include "quantize.cuh"
 #include "smallm.cuh"
@@ -20,6 +21,7 @@ namespace {
 
 namespace sm = nvfp4::smallm;
 namespace gt = nvfp4::gemvtc;
+namespace gb = nvfp4::gemvbf;
 
 // Weight and scale bytes one 16-row group brings per 256-k stage, and the
 // weight bytes an SM should keep in flight (HBM latency x its bandwidth share).
@@ -69,6 +71,7 @@ struct DeviceInfo {
   unsigned int* err = nullptr;         // device address of g_device_error
   int smallm_regs[2][5][sm::kMaxGroups + 1] = {};  // registers per thread by (f16, MT, G)
   int gemv_regs[2] = {};               // registers per thread of the tcgen05 few-row kernel (N 16, 32)
+  int gemv_bf16_regs[2][2] = {};       // the same, bf16 kernel, by (N 16 / 32, lane groups 2 / 4)
 };
 
 std::mutex g_mutex;
@@ -103,6 +106,20 @@ cudaError_t prepare_gemv(DeviceInfo& d) {
   if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, kern);
   if (e != cudaSuccess) return e;
   d.gemv_regs[NM == 16 ? 0 : 1] = fa.numRegs;
+  return cudaSuccess;
+}
+
+template <int NM, int NI>
+cudaError_t prepare_gemv_bf16(DeviceInfo& d) {
+  const auto kern = &gb::gemv_bf16_kernel<NM, NI>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, d.max_smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  cudaFuncAttributes fa;
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, kern);
+  if (e != cudaSuccess) return e;
+  d.gemv_bf16_regs[NM == 16 ? 0 : 1][NI == 2 ? 0 : 1] = fa.numRegs;
   return cudaSuccess;
 }
 
@@ -159,6 +176,10 @@ int device_setup(DeviceInfo** out) {
           prepare_smallm<4, false>(d) != cudaSuccess ||
           prepare_smallm<1, true>(d) != cudaSuccess ||
           prepare_gemv<16>(d) != cudaSuccess || prepare_gemv<32>(d) != cudaSuccess ||
+          prepare_gemv_bf16<16, 2>(d) != cudaSuccess ||
+          prepare_gemv_bf16<16, 4>(d) != cudaSuccess ||
+          prepare_gemv_bf16<32, 2>(d) != cudaSuccess ||
+          prepare_gemv_bf16<32, 4>(d) != cudaSuccess ||
           cudaFuncSetAttribute(nvfp4::tcgemm::tcgemm_kernel,
                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                nvfp4::tcgemm::kSmemBytes) != cudaSuccess) {
@@ -272,8 +293,7 @@ int validate(const void* x, const void* wp, const void* ws, const void* y, int64
   const unsigned int force = flags & (NVFP4_FLAG_FORCE_SMALLM | NVFP4_FLAG_FORCE_TCGEMM |
                                       NVFP4_FLAG_FORCE_GEMV);
   if (force & (force - 1)) return NVFP4_ERR_INVALID;        // at most one
-  if ((flags & NVFP4_FLAG_BF16_MMA) && (flags & (NVFP4_FLAG_FORCE_TCGEMM | NVFP4_FLAG_FORCE_GEMV)))
-    return NVFP4_ERR_INVALID;
+  if ((flags & NVFP4_FLAG_BF16_MMA) && (flags & NVFP4_FLAG_FORCE_TCGEMM)) return NVFP4_ERR_INVALID;
   if ((flags & (NVFP4_FLAG_FORCE_SMALLM | NVFP4_FLAG_FORCE_GEMV | NVFP4_FLAG_BF16_MMA)) &&
       M > kSmallMMax)
     return NVFP4_ERR_INVALID;
@@ -287,16 +307,23 @@ int validate(const void* x, const void* wp, const void* ws, const void* y, int64
   return NVFP4_OK;
 }
 
-// Kernel by M, from measurements on GB300 (graph-timed, the 5120 x 34816
-// projection): M <= 8 the warp-MMA kernel (f16) is fastest; M = 9..16 the
-// tcgen05 few-row kernel (2 CTAs per SM); M = 17..32 the warp-MMA kernel
-// again, where the tcgen05 one runs a single CTA per SM and its lone MMA
-// issuer (about 60 ns per tcgen05.mma whatever N is) bounds it.
-int kernel_for(int64_t M, unsigned int flags) {
-  if (flags & (NVFP4_FLAG_FORCE_SMALLM | NVFP4_FLAG_BF16_MMA)) return NVFP4_KERNEL_SMALLM;
+// Kernel by M (and, for M = 17..32, the weight size), from graph-timed
+// measurements on GB300: M <= 8 the warp-MMA kernel (f16) is fastest;
+// M = 9..16 the tcgen05 few-row kernel (f16, 2 CTAs per SM); M = 17..32 the
+// bf16 tcgen05 few-row kernel on large weight matrices (34816 x 5120:
+// 60 us against 77 us; 5120 x 17408: 39 against 51) and the warp-MMA kernel
+// (bf16) on smaller ones, where both take about as long and the warp MMA
+// is ahead (8192 x 5120: 19 us against 22).
+constexpr int64_t kBf16GemvMinWeights = int64_t(1) << 26;
+
+int kernel_for(int64_t M, int64_t N, int64_t K, unsigned int flags) {
+  if (flags & NVFP4_FLAG_FORCE_SMALLM) return NVFP4_KERNEL_SMALLM;
   if (flags & NVFP4_FLAG_FORCE_TCGEMM) return NVFP4_KERNEL_TCGEMM;
-  if (flags & NVFP4_FLAG_FORCE_GEMV) return NVFP4_KERNEL_GEMV;
+  if (flags & NVFP4_FLAG_FORCE_GEMV)
+    return (flags & NVFP4_FLAG_BF16_MMA) ? NVFP4_KERNEL_GEMV_BF16 : NVFP4_KERNEL_GEMV;
   if (M > kSmallMMax) return NVFP4_KERNEL_TCGEMM;
+  if (M > 16 && N * K >= kBf16GemvMinWeights) return NVFP4_KERNEL_GEMV_BF16;
+  if (flags & NVFP4_FLAG_BF16_MMA) return NVFP4_KERNEL_SMALLM;
   return (M > 8 && M <= 16) ? NVFP4_KERNEL_GEMV : NVFP4_KERNEL_SMALLM;
 }
 
@@ -541,6 +568,122 @@ int launch_gemv(const DeviceInfo& d, const void* x, const uint8_t* wp, const uin
   return NVFP4_OK;
 }
 
+struct GemvBfPlan {
+  int split = 0;
+  int stages = 0;
+  int64_t row_blocks = 0;
+  double cost = -1.0;
+};
+
+// The bf16 tcgen05 few-row kernel with NI lane groups: the deepest ring that
+// keeps exactly Roles::kCtasPerSm CTAs resident per SM (TMEM is split
+// between them), then the split as for plan_gemv.
+template <int NM, int NI>
+GemvBfPlan plan_gemv_bf16(const DeviceInfo& d, int64_t N, int64_t K, unsigned int flags) {
+  using R = gb::Roles<NM, NI>;
+  GemvBfPlan best;
+  const int64_t T = K / gb::kStageK;
+  const int want_split = (flags & NVFP4_FLAG_SPLIT_MASK) >> NVFP4_FLAG_SPLIT_SHIFT;
+  const int regs = d.gemv_bf16_regs[NM == 16 ? 0 : 1][NI == 2 ? 0 : 1];
+  int stages = 0;
+  for (int s = 2; s <= 12; ++s) {
+    const gb::SmemLayout lay = gb::make_layout(NM, NI, s);
+    if (lay.total > d.max_smem || !gb::layout_ok(lay, NM, NI)) continue;
+    if (resident_ctas(d, R::kThreads, regs, lay.total) == R::kCtasPerSm) stages = s;
+  }
+  if (stages == 0) return best;
+  best.row_blocks = N / gb::kRows;                  // SwiGLU: 64 gate + 64 up rows, same count
+  const int64_t slots = static_cast<int64_t>(d.num_sms) * R::kCtasPerSm;
+  int64_t best_ctas = 0;
+  bool best_one_wave = false;
+  const int s_max = static_cast<int>(std::min<int64_t>(T, gb::kMaxSplit));
+  for (int s = 1; s <= s_max; ++s) {
+    if (want_split && s != want_split) continue;
+    const int64_t ctas = best.row_blocks * s;
+    const bool one_wave = ctas <= slots;
+    const int64_t per_sm = (ctas + d.num_sms - 1) / d.num_sms;
+    const double cost = static_cast<double>(per_sm) * (static_cast<double>((T + s - 1) / s) + 1.5);
+    const bool better =
+        best.cost < 0 || (one_wave && !best_one_wave) ||
+        (one_wave == best_one_wave &&
+         (cost < best.cost * 0.999 || (cost <= best.cost * 1.001 && ctas < best_ctas)));
+    if (better) {
+      best.cost = cost;
+      best_ctas = ctas;
+      best_one_wave = one_wave;
+      best.split = s;
+    }
+  }
+  if (best.split > 0) best.stages = stages;
+  return best;
+}
+
+template <int NM, int NI>
+int launch_gemv_bf16(const DeviceInfo& d, const void* x, const uint8_t* wp, const uint8_t* ws,
+                     float gs, float gs_up, void* y, int64_t M, int64_t N, int64_t K,
+                     unsigned int flags, cudaStream_t stream, const SegSpec* segs) {
+  const GemvBfPlan plan = plan_gemv_bf16<NM, NI>(d, N, K, flags);
+  if (plan.stages == 0) return NVFP4_ERR_INVALID;   // an override that cannot run
+  CUtensorMap tw, ts, tx;
+  if (!encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, wp, K / 2, N, K / 2, 128, gb::kHalfRows,
+                 CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_2d(&ts, CU_TENSOR_MAP_DATA_TYPE_UINT8, ws, K / 16, N, K / 16, 16, gb::kHalfRows,
+                 CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !encode_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, K, M, K * 2, gb::kJobK, NM,
+                 CU_TENSOR_MAP_SWIZZLE_128B))
+    return NVFP4_ERR_LAUNCH;
+  gb::Params p;
+  p.y = y;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.out_scale = out_scale(gs);                      // the bf16 weights carry 2^-10
+  p.out_scale_up = out_scale(gs_up);
+  p.seg = seg_table(segs, static_cast<double>(nvfp4::kWeightPow2));
+  p.stages_total = static_cast<int>(K / gb::kStageK);
+  p.split = plan.split;
+  p.lay = gb::make_layout(NM, NI, plan.stages);
+  p.out_f32 = (flags & NVFP4_FLAG_F32_OUT) ? 1 : 0;
+  p.swiglu = (flags & NVFP4_FLAG_SWIGLU) ? 1 : 0;
+  p.err = d.err;
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof cfg);
+  cfg.gridDim = dim3(static_cast<unsigned>(plan.row_blocks), static_cast<unsigned>(plan.split), 1);
+  cfg.blockDim = dim3(gb::Roles<NM, NI>::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = p.lay.total;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = static_cast<unsigned>(plan.split);
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, gb::gemv_bf16_kernel<NM, NI>, tw, ts, tx, p);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return NVFP4_ERR_LAUNCH;
+  }
+  return NVFP4_OK;
+}
+
+// Lane groups: NVFP4_FLAG_GROUPS(2 | 4) pins them; otherwise two (two CTAs
+// per SM) when the row blocks alone fill the SMs, else four (one CTA per SM,
+// the larger TMEM share suits the k splits that fill the SMs then).
+template <int NM>
+int launch_gemv_bf16_any(const DeviceInfo& d, const void* x, const uint8_t* wp,
+                         const uint8_t* ws, float gs, float gs_up, void* y, int64_t M, int64_t N,
+                         int64_t K, unsigned int flags, cudaStream_t stream, const SegSpec* segs) {
+  int want = (flags & NVFP4_FLAG_GROUPS_MASK) >> NVFP4_FLAG_GROUPS_SHIFT;
+  if (want != 0 && want != 2 && want != 4) return NVFP4_ERR_INVALID;
+  if (want == 0) want = N / gb::kRows >= d.num_sms ? 2 : 4;
+  if (want == 2)
+    return launch_gemv_bf16<NM, 2>(d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs);
+  return launch_gemv_bf16<NM, 4>(d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs);
+}
+
 int launch_tcgemm(const DeviceInfo& d, const void* x, const uint8_t* wp, const uint8_t* ws,
                   float gs, float gs_up, void* y, int64_t M, int64_t N, int64_t K, unsigned int flags,
                   cudaStream_t stream, const SegSpec* segs) {
@@ -600,7 +743,12 @@ int run(const void* x, const uint8_t* wp, const uint8_t* ws, float gs, float gs_
   st = device_setup(&d);
   if (st != NVFP4_OK) return st;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
-  const int kernel = kernel_for(M, flags);
+  const int kernel = kernel_for(M, N, K, flags);
+  if (kernel == NVFP4_KERNEL_GEMV_BF16) {
+    if (M <= 16)
+      return launch_gemv_bf16_any<16>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs);
+    return launch_gemv_bf16_any<32>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs);
+  }
   if (kernel == NVFP4_KERNEL_GEMV) {
     if (M <= 16) return launch_gemv<16>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs);
     return launch_gemv<32>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs);
@@ -733,7 +881,7 @@ int nvfp4_linear_kernel_for(int64_t M, int64_t N, int64_t K, unsigned int flags)
   static const uint8_t dummy[16] __attribute__((aligned(16))) = {0};
   if (validate(dummy, dummy, dummy, dummy, M, N, K, flags) != NVFP4_OK || M == 0)
     return NVFP4_KERNEL_NONE;
-  return kernel_for(M, flags);
+  return kernel_for(M, N, K, flags);
 }
 
 int nvfp4_device_status(unsigned int* bits, int clear) {

@@ -31,7 +31,8 @@ def test_header_constants_match_binding():
                         ("NVFP4_FLAG_FORCE_TCGEMM", _lib.FLAG_FORCE_TCGEMM),
                         ("NVFP4_KERNEL_SMALLM", _lib.KERNEL_SMALLM),
                         ("NVFP4_KERNEL_TCGEMM", _lib.KERNEL_TCGEMM),
-                        ("NVFP4_KERNEL_GEMV", _lib.KERNEL_GEMV)):
+                        ("NVFP4_KERNEL_GEMV", _lib.KERNEL_GEMV),
+                        ("NVFP4_KERNEL_GEMV_BF16", _lib.KERNEL_GEMV_BF16)):
         assert "#define %s %du" % (name, value) in text or "#define %s %d " % (name, value) in text
     assert "#define NVFP4_FLAG_BF16_MMA (1u << 17)" in text and _lib.FLAG_BF16_MMA == 1 << 17
     assert "#define NVFP4_FLAG_FORCE_GEMV (1u << 18)" in text and _lib.FLAG_FORCE_GEMV == 1 << 18
@@ -52,12 +53,20 @@ def test_version_and_status_strings(lib):
     (9, 256, 512, 0, _lib.KERNEL_GEMV),
     (16, 256, 512, 0, _lib.KERNEL_GEMV),
     (17, 256, 512, 0, _lib.KERNEL_SMALLM),
-    (32, 34816, 5120, 0, _lib.KERNEL_SMALLM),
+    (32, 34816, 5120, 0, _lib.KERNEL_GEMV_BF16),                 # large layer, M = 17..32
+    (17, 5120, 17408, 0, _lib.KERNEL_GEMV_BF16),
+    (24, 8192, 5120, 0, _lib.KERNEL_SMALLM),                     # N * K < 2^26
+    (16, 34816, 5120, 0, _lib.KERNEL_GEMV),
+    (32, 34816, 5120, _lib.FLAG_BF16_MMA, _lib.KERNEL_GEMV_BF16),
+    (16, 34816, 5120, _lib.FLAG_BF16_MMA, _lib.KERNEL_SMALLM),
+    (7, 256, 512, _lib.FLAG_FORCE_GEMV | _lib.FLAG_BF16_MMA, _lib.KERNEL_GEMV_BF16),
+    (40, 256, 512, _lib.FLAG_FORCE_GEMV | _lib.FLAG_BF16_MMA, _lib.KERNEL_NONE),
     (1, 256, 512, _lib.FLAG_FORCE_SMALLM, _lib.KERNEL_SMALLM),
     (7, 256, 512, _lib.FLAG_BF16_MMA, _lib.KERNEL_SMALLM),
     (7, 256, 512, _lib.FLAG_FORCE_GEMV, _lib.KERNEL_GEMV),
     (40, 256, 512, _lib.FLAG_FORCE_GEMV, _lib.KERNEL_NONE),      # gemv needs M <= 32
     (7, 256, 512, _lib.FLAG_BF16_MMA | _lib.FLAG_FORCE_TCGEMM, _lib.KERNEL_NONE),
+    (7, 256, 512, _lib.FLAG_FORCE_GEMV | _lib.FLAG_FORCE_TCGEMM, _lib.KERNEL_NONE),
     (7, 256, 512, _lib.FLAG_FORCE_GEMV | _lib.FLAG_FORCE_SMALLM, _lib.KERNEL_NONE),
     (33, 34816, 5120, 0, _lib.KERNEL_TCGEMM),
     (8192, 34816, 5120, _lib.FLAG_SWIGLU, _lib.KERNEL_TCGEMM),

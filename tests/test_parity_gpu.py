@@ -56,8 +56,13 @@ def full_check(t, flags=0, what=""):
 
 
 # ------------------------------------------------------------------ small M
-# The two few-row kernels, each forced (the default picks one by M).
+# The few-row kernels, each forced (the default picks one by M): the tcgen05
+# kernel in f16 and in bf16 (with two and with four lane groups) and the
+# warp-MMA kernel.
+GEMV_BF16 = _lib.FLAG_FORCE_GEMV | _lib.FLAG_BF16_MMA
 FEW_ROW = [pytest.param(_lib.FLAG_FORCE_GEMV, id="gemv_tc"),
+           pytest.param(GEMV_BF16 | _lib.FLAG_GROUPS(4), id="gemv_bf16_g4"),
+           pytest.param(GEMV_BF16 | _lib.FLAG_GROUPS(2), id="gemv_bf16_g2"),
            pytest.param(_lib.FLAG_FORCE_SMALLM, id="smallm")]
 
 
@@ -65,7 +70,8 @@ FEW_ROW = [pytest.param(_lib.FLAG_FORCE_GEMV, id="gemv_tc"),
 @pytest.mark.parametrize("M", [1, 2, 5, 7, 8, 9, 16, 17, 24, 25, 31, 32])
 def test_few_row_all_row_counts(M, kflag):
     t = make_linear(M, 384, 1024, seed=100 + M)
-    want = _lib.KERNEL_SMALLM if kflag == _lib.FLAG_FORCE_SMALLM else _lib.KERNEL_GEMV
+    want = {_lib.FLAG_FORCE_SMALLM: _lib.KERNEL_SMALLM, _lib.FLAG_FORCE_GEMV: _lib.KERNEL_GEMV}.get(
+        kflag, _lib.KERNEL_GEMV_BF16)
     assert _lib.kernel_for(M, 384, 1024, kflag) == want
     assert _lib.kernel_for(M, 384, 1024) in (_lib.KERNEL_SMALLM, _lib.KERNEL_GEMV)
     full_check(t, kflag, what="few-row M=%d flags=%d" % (M, kflag))
@@ -97,6 +103,20 @@ def test_gemv_tc_every_split(M):
     for s in (1, 2, 3, 5, 7, 8, 16):
         _check_against(t, y64, a, _lib.FLAG_FORCE_GEMV | _lib.FLAG_SPLIT(s),
                        "gemv_tc M=%d split=%d" % (M, s))
+
+
+@pytest.mark.parametrize("M", [1, 7, 16, 17, 32])
+def test_gemv_bf16_every_split_and_group_count(M):
+    """The bf16 tcgen05 few-row kernel at every k split, with two and with
+    four lane groups: a CTA of 1..16 stages gives each group 1..64 jobs, so
+    every TMEM ring position and every stage-barrier parity is exercised."""
+    N, K = 640, 4096
+    t = make_linear(M, N, K, seed=1070 + M)
+    y64, a = _oracle(t)
+    for g in (2, 4):
+        for s in (1, 2, 3, 5, 7, 8, 16):
+            _check_against(t, y64, a, GEMV_BF16 | _lib.FLAG_GROUPS(g) | _lib.FLAG_SPLIT(s),
+                           "gemv_bf16 M=%d groups=%d split=%d" % (M, g, s))
 
 
 # ------------------------------------------------------------------ tcgen05
