@@ -235,7 +235,9 @@ def _wide_range_inputs(M, seed):
                                      (4, _lib.FLAG_FORCE_SMALLM),
                                      (4, _lib.FLAG_FORCE_SMALLM | _lib.FLAG_SPLIT(8)),
                                      (8, _lib.FLAG_FORCE_SMALLM | _lib.FLAG_SPLIT(3)),
-                                     (12, _lib.FLAG_FORCE_SMALLM)])
+                                     (12, _lib.FLAG_FORCE_SMALLM),
+                                     (4, GEMV_BF16), (32, GEMV_BF16 | _lib.FLAG_GROUPS(2)),
+                                     (24, GEMV_BF16 | _lib.FLAG_SPLIT(3))])
 def test_wide_dynamic_range_rows(M, flags):
     t = _wide_range_inputs(M, seed=1300 + M)
     y64, a = _oracle(t)
@@ -251,7 +253,9 @@ def test_wide_dynamic_range_rows(M, flags):
 @pytest.mark.parametrize("M,flags", [(1, 0), (6, 0), (6, _lib.FLAG_BF16_MMA), (20, 0),
                                      (1, _lib.FLAG_FORCE_SMALLM), (6, _lib.FLAG_FORCE_SMALLM),
                                      (1, _lib.FLAG_FORCE_GEMV), (6, _lib.FLAG_FORCE_GEMV),
-                                     (6, _lib.FLAG_FORCE_TCGEMM), (50, 0)])
+                                     (6, _lib.FLAG_FORCE_TCGEMM), (50, 0),
+                                     (1, GEMV_BF16), (6, GEMV_BF16),
+                                     (20, GEMV_BF16 | _lib.FLAG_GROUPS(2))])
 def test_non_finite_values_propagate(M, flags):
     """An inf or NaN activation, or a NaN block scale (e4m3 S.1111.111),
     gives the non-finite outputs the exact sum gives (IEEE: inf * 0 = NaN,
@@ -282,7 +286,8 @@ def test_non_finite_values_propagate(M, flags):
 
 
 @pytest.mark.parametrize("M,kflag", [(1, 0), (7, _lib.FLAG_FORCE_SMALLM), (12, 0), (24, 0),
-                                     (7, _lib.FLAG_FORCE_GEMV), (64, 0), (300, 0)])
+                                     (7, _lib.FLAG_FORCE_GEMV), (64, 0), (300, 0),
+                                     (7, GEMV_BF16), (24, GEMV_BF16 | _lib.FLAG_GROUPS(2))])
 def test_swiglu_separate_gate_up_global_scales(M, kflag):
     """Gate rows with one global scale, up rows with another: equal to the
     oracle's two half-linears combined by SwiGLU."""
@@ -310,7 +315,8 @@ def test_swiglu_separate_gate_up_global_scales(M, kflag):
 
 
 @pytest.mark.parametrize("M,kflag", [(1, 0), (7, 0), (7, _lib.FLAG_FORCE_GEMV), (12, 0),
-                                     (32, 0), (100, 0)])
+                                     (32, 0), (100, 0), (7, GEMV_BF16),
+                                     (32, GEMV_BF16 | _lib.FLAG_GROUPS(4))])
 def test_segmented_qkv_global_scales(M, kflag):
     """q, k and v stacked into one launch, each with its own global scale:
     equal to three separate oracle linears side by side (segments of 384,
@@ -351,7 +357,8 @@ def _exhaustive_products():
 
 
 @pytest.mark.parametrize("flags", [_lib.FLAG_FORCE_SMALLM, _lib.FLAG_FORCE_TCGEMM,
-                                   _lib.FLAG_FORCE_GEMV])
+                                   _lib.FLAG_FORCE_GEMV, GEMV_BF16,
+                                   GEMV_BF16 | _lib.FLAG_GROUPS(2)])
 def test_every_code_times_every_scale_is_exact(flags):
     t = _exhaustive_products()
     y64, _ = oracle.linear_f64(t.x_bits, t.w_packed, t.w_scale, t.global_scale)
@@ -362,7 +369,8 @@ def test_every_code_times_every_scale_is_exact(flags):
 
 
 @pytest.mark.parametrize("M,flags", [(5, 0), (12, 0), (30, 0), (70, 0),
-                                     (5, _lib.FLAG_FORCE_TCGEMM), (5, _lib.FLAG_FORCE_GEMV)])
+                                     (5, _lib.FLAG_FORCE_TCGEMM), (5, _lib.FLAG_FORCE_GEMV),
+                                     (5, GEMV_BF16), (30, GEMV_BF16 | _lib.FLAG_GROUPS(2))])
 def test_exact_integer_inputs_are_bit_exact(M, flags):
     # small-integer activations, power-of-two scales, global scale 1: every
     # partial sum is an exactly representable fp32 number, so the result is
@@ -379,7 +387,7 @@ def test_exact_integer_inputs_are_bit_exact(M, flags):
     assert np.array_equal(y32, y64)
 
 
-@pytest.mark.parametrize("M,flags", [(3, 0), (3, _lib.FLAG_FORCE_GEMV), (50, 0)])
+@pytest.mark.parametrize("M,flags", [(3, 0), (3, _lib.FLAG_FORCE_GEMV), (50, 0), (3, GEMV_BF16)])
 def test_sign_flip_negates_exactly(M, flags):
     t = make_linear(M, 256, 512, seed=600 + M)
     y = run(t, _lib.FLAG_F32_OUT | flags).cpu().numpy()
@@ -388,7 +396,8 @@ def test_sign_flip_negates_exactly(M, flags):
     assert np.array_equal(y_neg, -y)
 
 
-@pytest.mark.parametrize("M,flags", [(1, 0), (1, _lib.FLAG_FORCE_GEMV), (40, 0)])
+@pytest.mark.parametrize("M,flags", [(1, 0), (1, _lib.FLAG_FORCE_GEMV), (40, 0), (1, GEMV_BF16),
+                                     (32, GEMV_BF16)])
 def test_nibble_order(M, flags):
     K, N = 256, 128
     x = np.zeros((M, K), np.uint16)
@@ -575,3 +584,38 @@ def test_full_size_workloads_sampled(name):
             check_bf16(ybs, y64, a, oracle.to_bf16_bits(y64), "%s/%s" % (name, t.name))
         del x, wp, ws, y32, ybf
         torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("M,swiglu", [(20, False), (32, True)])
+def test_bf16_few_row_kernel_is_the_default_on_large_layers(M, swiglu):
+    """M = 17..32 on a weight matrix of N * K = 2^26 runs the bf16 tcgen05
+    few-row kernel by default (two lane groups: 128 row blocks fill the
+    SMs); sampled outputs against the oracle."""
+    N, K = 16384, 4096
+    flags = _lib.FLAG_SWIGLU if swiglu else 0
+    assert _lib.kernel_for(M, N, K, flags) == _lib.KERNEL_GEMV_BF16
+    t = make_linear(M, N, K, seed=2100 + M)
+    x, wp, ws = to_dev(t)
+    y32 = _lib.linear_ex(x, wp, ws, float(t.global_scale), flags | _lib.FLAG_F32_OUT)
+    ybf = _lib.linear_ex(x, wp, ws, float(t.global_scale), flags)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(2200 + M)
+    n_out = y32.shape[1]
+    mi = rng.integers(0, M, size=800)
+    ni = rng.integers(0, n_out, size=800)
+    y32s = y32.cpu().numpy()[mi, ni].astype(np.float64)
+    ybs = bf16_bits(ybf)[mi, ni]
+    if swiglu:
+        H = N // 2
+        g64, ga = oracle.linear_points_f64(t.x_bits, t.w_packed, t.w_scale, t.global_scale, mi, ni)
+        u64, ua = oracle.linear_points_f64(t.x_bits, t.w_packed, t.w_scale, t.global_scale, mi,
+                                           ni + H)
+        y64, a = np.stack([g64, u64], 1), np.stack([ga, ua], 1)
+        out64 = oracle.swiglu_f64(y64)[:, 0]
+        check_swiglu_f32(y32s[:, None], y64, a, out64[:, None], "bf16 default swiglu")
+        check_swiglu_bf16(ybs[:, None], y64, a, out64[:, None],
+                          oracle.to_bf16_bits(out64)[:, None], "bf16 default swiglu")
+    else:
+        y64, a = oracle.linear_points_f64(t.x_bits, t.w_packed, t.w_scale, t.global_scale, mi, ni)
+        check_f32(y32s, y64, a, "bf16 default M=%d" % M)
+        check_bf16(ybs, y64, a, oracle.to_bf16_bits(y64), "bf16 default M=%d" % M)
