@@ -123,6 +123,21 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity,
   return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag));
 }
 
+// Position of a stage in the ring (slot and barrier parity), walked forward
+// stage by stage: the ring depth is a launch parameter, and a division by
+// it per job measurably slowed the dequantisers.
+struct RingPos {
+  int stage = 0, slot = 0;
+  uint32_t parity = 0;
+  __device__ __forceinline__ void advance_to(int target, int depth) {
+    for (; stage < target; ++stage)
+      if (++slot == depth) {
+        slot = 0;
+        parity ^= 1u;
+      }
+  }
+};
+
 template <int NM, int NI>
 __global__ void __launch_bounds__(Roles<NM, NI>::kThreads, Roles<NM, NI>::kCtasPerSm)
     gemv_bf16_kernel(const __grid_constant__ CUtensorMap tm_w,
@@ -262,10 +277,12 @@ __global__ void __launch_bounds__(Roles<NM, NI>::kThreads, Roles<NM, NI>::kCtasP
       const uint32_t d_tmem = tmem + R::kDCol + gi * NM;
       int n = 0, aslot = 0;
       uint32_t apar = 0;
+      RingPos pos;
       for (int j = gi; j < n_jobs_total; j += NI, ++n) {
-        const int s = j / kJobsPerStage, q = j % kJobsPerStage;
-        const int slot = s % S;
-        if (!mbar_wait(&full[slot], static_cast<uint32_t>(s / S) & 1u, abort_flag)) break;
+        const int q = j % kJobsPerStage;
+        pos.advance_to(j / kJobsPerStage, S);
+        const int slot = pos.slot;
+        if (!mbar_wait(&full[slot], pos.parity, abort_flag)) break;
         if (!mbar_wait(&a_full[gi * kSlotsPerGroup + aslot], apar, abort_flag)) break;
         tc_fence_after_sync();
         const uint64_t b_desc0 =
@@ -294,15 +311,16 @@ __global__ void __launch_bounds__(Roles<NM, NI>::kThreads, Roles<NM, NI>::kCtasP
     const int row = 32 * qd + lane;
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(32 * qd) << 16);
     int n = 0, aslot = 0;
+    RingPos pos, prev;          // this job's stage; the stage of the slot's previous job
     for (int j = gi; j < n_jobs_total; j += NI, ++n) {
-      const int s = j / kJobsPerStage, q = j % kJobsPerStage;
-      const int slot = s % S;
-      if (!warp_wait(&full[slot], static_cast<uint32_t>(s / S) & 1u, abort_flag)) break;
+      const int q = j % kJobsPerStage;
+      pos.advance_to(j / kJobsPerStage, S);
+      const int slot = pos.slot;
+      if (!warp_wait(&full[slot], pos.parity, abort_flag)) break;
       if (n >= kSlotsPerGroup) {
         // the slot's previous job (kSlotsPerGroup jobs back) must be done
-        const int s_prev = (j - NI * kSlotsPerGroup) / kJobsPerStage;
-        if (!warp_wait(&empty[s_prev % S], static_cast<uint32_t>(s_prev / S) & 1u, abort_flag))
-          break;
+        prev.advance_to((j - NI * kSlotsPerGroup) / kJobsPerStage, S);
+        if (!warp_wait(&empty[prev.slot], prev.parity, abort_flag)) break;
       }
       const uint8_t* st = smem + slot * L.stage_bytes;
       // 64 k = code chunks 2q, 2q+1 of the row's 128-byte swizzled line

@@ -311,7 +311,7 @@ int validate(const void* x, const void* wp, const void* ws, const void* y, int64
 // measurements on GB300: M <= 8 the warp-MMA kernel (f16) is fastest;
 // M = 9..16 the tcgen05 few-row kernel (f16, 2 CTAs per SM); M = 17..32 the
 // bf16 tcgen05 few-row kernel on large weight matrices (34816 x 5120:
-// 60 us against 77 us; 5120 x 17408: 39 against 51) and the warp-MMA kernel
+// 54 us against 76 us; 5120 x 17408: 39 against 51) and the warp-MMA kernel
 // (bf16) on smaller ones, where both take about as long and the warp MMA
 // is ahead (8192 x 5120: 19 us against 22).
 constexpr int64_t kBf16GemvMinWeights = int64_t(1) << 26;
