@@ -15,11 +15,19 @@
 // Three stream-ordered steps, no workspace: the tensor maximum is gathered
 // by atomicMax into the caller's global-scale word (as fp32 bits: the bit
 // patterns of non-negative floats order like their values), the quantiser
-// reads it, and a last one-thread kernel turns it into 448 / amax.  The
-// quantiser streams its input once: HBM-bound.
+// reads it, and a last one-thread kernel turns it into 448 / amax.
+//
+// The per-weight division by the block scale is done without a general fp32
+// division, which dominated the quantiser's instruction count: an e4m3 scale
+// is s = d * 2^e with d an odd integer <= 15, so RN(v / s) = RN(v / d) * 2^-e
+// (exact scaling while the quotient is a normal number; a smaller quotient
+// is far below every e2m1 rounding threshold), and RN(v / d) follows from the
+// correctly rounded reciprocal r = RN(1/d) by Markstein's refinement,
+// q0 = RN(v r), rem = RN(v - q0 d), q1 = RN(q0 + rem r), which is correctly
+// rounded for every fp32 v and every such d (checked exhaustively over all
+// significands in the tests).
 #pragma once
 #include <cstdint>
-#include <cuda_fp16.h>
 
 #include "ptx.cuh"
 
@@ -56,21 +64,38 @@ __device__ __forceinline__ float global_scale_of(float amax) {
   return amax > 0.0f ? __fdiv_rn(448.0f, amax) : 1.0f;
 }
 
-// e4m3 bits of the nearest e4m3 to v (saturating), and their value.
+// e4m3 bits of the nearest e4m3 to v (saturating).
 __device__ __forceinline__ uint32_t to_e4m3(float v) {
   uint16_t d;
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(0.0f), "f"(v));
   return d & 0xFFu;
 }
-__device__ __forceinline__ float from_e4m3(uint32_t b) {
-  uint32_t h;
-  asm("{\n\t.reg .b16 s;\n\t"
-      "cvt.u16.u32 s, %1;\n\t"
-      "cvt.rn.f16x2.e4m3x2 %0, s;\n\t}"
-      : "=r"(h)
-      : "r"(b));
-  return __half2float(__ushort_as_half(static_cast<unsigned short>(h & 0xFFFFu)));
+// A block scale (finite, nonzero e4m3 byte b) as d * 2^e, d odd: the
+// divisor d, r = RN(1/d) and the factor 2^-e.
+struct ScaleDiv {
+  float d, r, p2;
+};
+__device__ __forceinline__ ScaleDiv scale_div(uint32_t b) {
+  const int E = static_cast<int>((b >> 3) & 15u), m = static_cast<int>(b & 7u);
+  const int sig = E ? 8 + m : m;                 // s = sig * 2^ex
+  const int ex = E ? E - 10 : -9;
+  const int t = __ffs(sig) - 1;                  // trailing zero bits of sig
+  const int e = ex + t;                          // in [-9, 8]
+  ScaleDiv sd;
+  sd.d = static_cast<float>(sig >> t);
+  sd.r = __frcp_rn(sd.d);
+  sd.p2 = __int_as_float((127 - e) << 23);
+  return sd;
 }
+// RN(v / s) for the scale split by scale_div (v finite); the sign of a zero
+// quotient follows v, as in the division.
+__device__ __forceinline__ float div_by_scale(float v, const ScaleDiv& sd) {
+  const float q0 = __fmul_rn(v, sd.r);
+  const float rem = __fmaf_rn(-q0, sd.d, v);
+  const float q1 = __fmaf_rn(rem, sd.r, q0);
+  return copysignf(__fmul_rn(q1, sd.p2), v);
+}
+
 // Two codes in one byte: lo -> low nibble (even k), hi -> high nibble.
 __device__ __forceinline__ uint32_t to_e2m1x2(float lo, float hi) {
   uint32_t d;
@@ -101,13 +126,15 @@ __global__ void __launch_bounds__(kThreads)
       amax_b = fmaxf(amax_b, fmaxf(fabsf(f[2 * i]), fabsf(f[2 * i + 1])));
     }
     const uint32_t sbyte = to_e4m3(__fdiv_rn(__fmul_rn(amax_b, gs), 6.0f));
-    const float s = from_e4m3(sbyte);
     uint32_t packed[2] = {0u, 0u};
-    if (s != 0.0f) {
+    // zero scale: all codes +0; a NaN scale (only from non-finite weights,
+    // which the format does not cover) likewise
+    if (sbyte != 0u && sbyte != 0x7Fu) {
+      const ScaleDiv sd = scale_div(sbyte);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const uint32_t byte = to_e2m1x2(__fdiv_rn(__fmul_rn(f[2 * i], gs), s),
-                                        __fdiv_rn(__fmul_rn(f[2 * i + 1], gs), s));
+        const uint32_t byte = to_e2m1x2(div_by_scale(__fmul_rn(f[2 * i], gs), sd),
+                                        div_by_scale(__fmul_rn(f[2 * i + 1], gs), sd));
         packed[i >> 2] |= byte << (8 * (i & 3));
       }
     }
