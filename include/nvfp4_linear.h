@@ -84,19 +84,19 @@ extern "C" {
 #define NVFP4_FLAG_GROUPS_MASK (0xFu << NVFP4_FLAG_GROUPS_SHIFT)
 #define NVFP4_FLAG_GROUPS(n) (((unsigned int)(n) & 0xFu) << NVFP4_FLAG_GROUPS_SHIFT)
 /* Multiply in bf16, the activations as given (exact for any activations;
- * M <= 32): the warp-MMA few-row kernel, or with NVFP4_FLAG_FORCE_GEMV the
- * bf16 tcgen05 few-row kernel (which M = 17..32 uses by default on weight
- * matrices of N * K >= 2^26).  Without it, the default few-row kernels for
- * M <= 16 multiply in f16: code * scale is exact in f16, and each
+ * M <= 32): at M <= 8 the warp-MMA few-row kernel in bf16 instead of f16;
+ * with NVFP4_FLAG_FORCE_GEMV the bf16 tcgen05 few-row kernel.  (Every
+ * default for M = 9..32 is already bf16: the bf16 tcgen05 kernel on weight
+ * matrices of N * K >= 2^26, the warp-MMA kernel otherwise.)  Without it,
+ * M <= 8 multiplies in f16: code * scale is exact in f16, and each
  * activation row is brought to f16 after scaling by a power of two taken
- * from the row's maximum |x| (the warp-MMA kernel: running maximum; the
- * tcgen05 kernel: maximum within each 256-k stage), which is exact for
- * every activation within a factor 2^31 of that maximum and otherwise
- * rounds it like an f16 subnormal.  (The warp-MMA kernel uses f16 only for
- * M <= 8.) */
+ * from the row's running maximum |x|, which is exact for every activation
+ * within a factor 2^31 of that maximum and otherwise rounds it like an f16
+ * subnormal.  The f16 tcgen05 few-row kernel (only when forced) does the
+ * same with the maximum within each 256-k stage. */
 #define NVFP4_FLAG_BF16_MMA (1u << 17)
-/* Force the tcgen05 few-row kernel (needs M <= 32): in f16, or in bf16
- * with NVFP4_FLAG_BF16_MMA. */
+/* Force a tcgen05 few-row kernel (needs M <= 32): the f16 one, or with
+ * NVFP4_FLAG_BF16_MMA the bf16 one. */
 #define NVFP4_FLAG_FORCE_GEMV (1u << 18)
 
 /* Kernel identifiers returned by nvfp4_linear_kernel_for. */

@@ -1,6 +1,8 @@
 // gemv_tc.cuh -- NVFP4 W4A16 linear for few activation rows (M <= 32):
 // decode (M = 1), speculative verify (M = K+1, FlashRT docs section 3) and
-// small continuous batches, on the tcgen05 tensor cores.
+// small continuous batches, on the tcgen05 tensor cores, in f16.  (Run when
+// forced: the bf16 kernel of gemv_bf16.cuh and the warp-MMA kernel are the
+// defaults; this one is kept for its f16 arithmetic and per-stage exponents.)
 //
 // At these sizes the layer is bound by streaming the packed weights and
 // scales from HBM once.  What limits a kernel that keeps up with HBM is the

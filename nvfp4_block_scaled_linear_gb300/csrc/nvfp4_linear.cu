@@ -307,13 +307,16 @@ int validate(const void* x, const void* wp, const void* ws, const void* y, int64
   return NVFP4_OK;
 }
 
-// Kernel by M (and, for M = 17..32, the weight size), from graph-timed
-// measurements on GB300: M <= 8 the warp-MMA kernel (f16) is fastest;
-// M = 9..16 the tcgen05 few-row kernel (f16, 2 CTAs per SM); M = 17..32 the
-// bf16 tcgen05 few-row kernel on large weight matrices (34816 x 5120:
-// 54 us against 76 us; 5120 x 17408: 39 against 51) and the warp-MMA kernel
-// (bf16) on smaller ones, where both take about as long and the warp MMA
-// is ahead (8192 x 5120: 19 us against 22).
+// Kernel by M (and, for M = 9..32, the weight size), from graph-timed
+// measurements on GB300: M <= 8 the warp-MMA kernel in f16 (decode 21.8 us
+// against 29.5-32 us for the tcgen05 few-row kernels); M = 9..32 the bf16
+// tcgen05 few-row kernel on large weight matrices (M = 32: 34816 x 5120 in
+// 54 us against 76 us, 5120 x 17408 in 39 against 51; M = 16: 49 against 55
+// and 34 against 35) and the warp-MMA kernel in bf16 on smaller ones (M = 16,
+// 8192 x 5120: 16 us against 18).  The f16 tcgen05 few-row kernel, 3-8%
+// ahead only at M = 9..12 on the largest shape and up to 1.7x behind
+// elsewhere, runs only when forced.  Every default above M = 8 multiplies
+// the activations exactly (bf16).
 constexpr int64_t kBf16GemvMinWeights = int64_t(1) << 26;
 
 int kernel_for(int64_t M, int64_t N, int64_t K, unsigned int flags) {
@@ -322,9 +325,8 @@ int kernel_for(int64_t M, int64_t N, int64_t K, unsigned int flags) {
   if (flags & NVFP4_FLAG_FORCE_GEMV)
     return (flags & NVFP4_FLAG_BF16_MMA) ? NVFP4_KERNEL_GEMV_BF16 : NVFP4_KERNEL_GEMV;
   if (M > kSmallMMax) return NVFP4_KERNEL_TCGEMM;
-  if (M > 16 && N * K >= kBf16GemvMinWeights) return NVFP4_KERNEL_GEMV_BF16;
-  if (flags & NVFP4_FLAG_BF16_MMA) return NVFP4_KERNEL_SMALLM;
-  return (M > 8 && M <= 16) ? NVFP4_KERNEL_GEMV : NVFP4_KERNEL_SMALLM;
+  if (M > 8 && N * K >= kBf16GemvMinWeights) return NVFP4_KERNEL_GEMV_BF16;
+  return NVFP4_KERNEL_SMALLM;
 }
 
 struct SmallmPlan {

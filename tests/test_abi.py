@@ -50,15 +50,18 @@ def test_version_and_status_strings(lib):
 @pytest.mark.parametrize("M,N,K,flags,expect", [
     (1, 256, 512, 0, _lib.KERNEL_SMALLM),
     (8, 256, 512, 0, _lib.KERNEL_SMALLM),
-    (9, 256, 512, 0, _lib.KERNEL_GEMV),
-    (16, 256, 512, 0, _lib.KERNEL_GEMV),
+    (9, 256, 512, 0, _lib.KERNEL_SMALLM),
+    (16, 256, 512, 0, _lib.KERNEL_SMALLM),
+    (9, 34816, 5120, 0, _lib.KERNEL_GEMV_BF16),
+    (8, 34816, 5120, 0, _lib.KERNEL_SMALLM),
     (17, 256, 512, 0, _lib.KERNEL_SMALLM),
     (32, 34816, 5120, 0, _lib.KERNEL_GEMV_BF16),                 # large layer, M = 17..32
     (17, 5120, 17408, 0, _lib.KERNEL_GEMV_BF16),
     (24, 8192, 5120, 0, _lib.KERNEL_SMALLM),                     # N * K < 2^26
-    (16, 34816, 5120, 0, _lib.KERNEL_GEMV),
+    (16, 34816, 5120, 0, _lib.KERNEL_GEMV_BF16),
     (32, 34816, 5120, _lib.FLAG_BF16_MMA, _lib.KERNEL_GEMV_BF16),
-    (16, 34816, 5120, _lib.FLAG_BF16_MMA, _lib.KERNEL_SMALLM),
+    (16, 34816, 5120, _lib.FLAG_BF16_MMA, _lib.KERNEL_GEMV_BF16),
+    (8, 34816, 5120, _lib.FLAG_BF16_MMA, _lib.KERNEL_SMALLM),
     (7, 256, 512, _lib.FLAG_FORCE_GEMV | _lib.FLAG_BF16_MMA, _lib.KERNEL_GEMV_BF16),
     (40, 256, 512, _lib.FLAG_FORCE_GEMV | _lib.FLAG_BF16_MMA, _lib.KERNEL_NONE),
     (1, 256, 512, _lib.FLAG_FORCE_SMALLM, _lib.KERNEL_SMALLM),
