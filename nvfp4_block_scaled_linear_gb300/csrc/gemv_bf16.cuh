@@ -77,7 +77,7 @@ struct SmemLayout {
 };
 
 __host__ __device__ constexpr int num_barriers(int stages, int ni) {
-  return 2 * stages + ni * kSlotsPerGroup + 1;
+  return 2 * stages + 2 * ni * kSlotsPerGroup + 1;
 }
 
 __host__ __device__ constexpr SmemLayout make_layout(int nm, int ni, int stages) {
@@ -92,14 +92,9 @@ __host__ __device__ constexpr SmemLayout make_layout(int nm, int ni, int stages)
   return l;
 }
 
-// A dequantisation warp waits for the stage of its job kSlotsPerGroup jobs
-// back on that stage's `empty` barrier; for the parity to be unambiguous the
-// barrier must not have moved on by two phases, which holds while a lane
-// group's ring is shallower than the jobs it sees in stages - 1 stages.  The
-// final exchange reuses the ring; it must fit.
-__host__ __device__ constexpr bool layout_ok(const SmemLayout& l, int nm, int ni) {
-  return l.stages >= 2 && kSlotsPerGroup * ni <= kJobsPerStage * (l.stages - 1) &&
-         kRows * nm * 4 <= l.stages * l.stage_bytes;
+// The final exchange reuses the ring; it must fit.
+__host__ __device__ constexpr bool layout_ok(const SmemLayout& l, int nm) {
+  return l.stages >= 2 && kRows * nm * 4 <= l.stages * l.stage_bytes;
 }
 
 struct Params {
@@ -154,11 +149,14 @@ __global__ void __launch_bounds__(Roles<NM, NI>::kThreads, Roles<NM, NI>::kCtasP
   uint32_t* lut = reinterpret_cast<uint32_t*>(smem + L.lut_off);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bar_off);   // TMA landed
   // Stage consumed: every issuer has committed its last job of the stage
-  // (one tcgen05.commit per stage and issuer).  It releases the ring slot to
-  // the producer and the stage's TMEM weight slots to the dequantisers.
+  // (one tcgen05.commit per stage and issuer); releases the ring slot.
   uint64_t* empty = full + S;
   uint64_t* a_full = empty + S;                  // [NI][3] TMEM weights written
-  uint64_t* mma_done = a_full + NI * kSlotsPerGroup;   // every MMA has completed
+  // [NI][3] the slot's MMAs have completed (one commit per job): releases
+  // the TMEM slot to its group's dequantisers, so that the groups do not
+  // wait for each other (a wait on the stage barrier had them in lockstep).
+  uint64_t* a_empty = a_full + NI * kSlotsPerGroup;
+  uint64_t* mma_done = a_empty + NI * kSlotsPerGroup;  // every MMA has completed
   volatile int* abort_flag = reinterpret_cast<volatile int*>(mma_done + 1);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1) + 1;
 
@@ -189,7 +187,10 @@ __global__ void __launch_bounds__(Roles<NM, NI>::kThreads, Roles<NM, NI>::kCtasP
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], NI);
     }
-    for (int a = 0; a < NI * kSlotsPerGroup; ++a) mbar_init(&a_full[a], 4);
+    for (int a = 0; a < NI * kSlotsPerGroup; ++a) {
+      mbar_init(&a_full[a], 4);
+      mbar_init(&a_empty[a], 1);
+    }
     mbar_init(mma_done, NI);
     *abort_flag = 0;
     fence_mbar_init();
@@ -269,8 +270,9 @@ __global__ void __launch_bounds__(Roles<NM, NI>::kThreads, Roles<NM, NI>::kCtasP
   } else if (warp < R::kWarpDeq) {
     // ------------------------------------------------------------ MMA issue
     // Issuer i takes jobs i, i + NI, ...: job j is k [64 (j % 4), +64) of
-    // stage j / 4, four MMAs of K = 16 into accumulator i.  It commits once
-    // per stage, after its last job there.
+    // stage j / 4, four MMAs of K = 16 into accumulator i.  It commits each
+    // job to the job's TMEM slot and, after its last job of a stage, to the
+    // stage.
     const int gi = warp - R::kWarpMma;
     if (lane == 0) {
       constexpr uint32_t idesc = umma_idesc_bf16(kRows, NM);
@@ -292,6 +294,7 @@ __global__ void __launch_bounds__(Roles<NM, NI>::kThreads, Roles<NM, NI>::kCtasP
         for (int kk = 0; kk < kJobK / 16; ++kk)
           umma_f16_tmem_a(d_tmem, a_tmem + kk * 8, b_desc0 + static_cast<uint64_t>((kk * 32) >> 4),
                           idesc, (n > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&a_empty[gi * kSlotsPerGroup + aslot]);
         if (q + NI >= kJobsPerStage) umma_commit(&empty[slot]);
         if (++aslot == kSlotsPerGroup) {
           aslot = 0;
@@ -311,17 +314,16 @@ __global__ void __launch_bounds__(Roles<NM, NI>::kThreads, Roles<NM, NI>::kCtasP
     const int row = 32 * qd + lane;
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(32 * qd) << 16);
     int n = 0, aslot = 0;
-    RingPos pos, prev;          // this job's stage; the stage of the slot's previous job
+    uint32_t epar = 0;          // parity of the slot's previous use
+    RingPos pos;
     for (int j = gi; j < n_jobs_total; j += NI, ++n) {
       const int q = j % kJobsPerStage;
       pos.advance_to(j / kJobsPerStage, S);
       const int slot = pos.slot;
       if (!warp_wait(&full[slot], pos.parity, abort_flag)) break;
-      if (n >= kSlotsPerGroup) {
-        // the slot's previous job (kSlotsPerGroup jobs back) must be done
-        prev.advance_to((j - NI * kSlotsPerGroup) / kJobsPerStage, S);
-        if (!warp_wait(&empty[prev.slot], prev.parity, abort_flag)) break;
-      }
+      if (n >= kSlotsPerGroup &&
+          !warp_wait(&a_empty[gi * kSlotsPerGroup + aslot], epar, abort_flag))
+        break;          // the slot's previous job (kSlotsPerGroup jobs back) not done
       const uint8_t* st = smem + slot * L.stage_bytes;
       // 64 k = code chunks 2q, 2q+1 of the row's 128-byte swizzled line
       const uint4 w0 =
@@ -347,7 +349,10 @@ __global__ void __launch_bounds__(Roles<NM, NI>::kThreads, Roles<NM, NI>::kCtasP
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(&a_full[gi * kSlotsPerGroup + aslot]);
-      if (++aslot == kSlotsPerGroup) aslot = 0;
+      if (++aslot == kSlotsPerGroup) {
+        aslot = 0;
+        if (n + 1 > kSlotsPerGroup) epar ^= 1u;   // from the second round on
+      }
     }
   }
 

@@ -311,10 +311,10 @@ int validate(const void* x, const void* wp, const void* ws, const void* y, int64
 // measurements on GB300: M <= 8 the warp-MMA kernel in f16 (decode 21.8 us
 // against 29.5-32 us for the tcgen05 few-row kernels); M = 9..32 the bf16
 // tcgen05 few-row kernel on large weight matrices (M = 32: 34816 x 5120 in
-// 54 us against 76 us, 5120 x 17408 in 39 against 51; M = 16: 49 against 55
-// and 34 against 35) and the warp-MMA kernel in bf16 on smaller ones (M = 16,
-// 8192 x 5120: 16 us against 18).  The f16 tcgen05 few-row kernel, 3-8%
-// ahead only at M = 9..12 on the largest shape and up to 1.7x behind
+// 53 us against 77 us, 5120 x 17408 in 37 against 51; M = 16: 48 against 55
+// and 33 against 35) and the warp-MMA kernel in bf16 on smaller ones (M = 16,
+// 8192 x 5120: 16 us against 18).  The f16 tcgen05 few-row kernel, 0-6%
+// ahead only at M = 9..12 on the largest shape and up to 1.8x behind
 // elsewhere, runs only when forced.  Every default above M = 8 multiplies
 // the activations exactly (bf16).
 constexpr int64_t kBf16GemvMinWeights = int64_t(1) << 26;
@@ -590,7 +590,7 @@ GemvBfPlan plan_gemv_bf16(const DeviceInfo& d, int64_t N, int64_t K, unsigned in
   int stages = 0;
   for (int s = 2; s <= 12; ++s) {
     const gb::SmemLayout lay = gb::make_layout(NM, NI, s);
-    if (lay.total > d.max_smem || !gb::layout_ok(lay, NM, NI)) continue;
+    if (lay.total > d.max_smem || !gb::layout_ok(lay, NM)) continue;
     if (resident_ctas(d, R::kThreads, regs, lay.total) == R::kCtasPerSm) stages = s;
   }
   if (stages == 0) return best;
