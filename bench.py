@@ -334,12 +334,13 @@ def time_case(case, steps, warmup, stream, world, sampler=None, graph=True):
 
 
 def e2e_case(case, steps, stream, dev):
-    """Same workload through the public API (the eager Python call) with the
-    step's data in host memory: every step copies its activations in from
-    pinned host memory, calls the layer and copies its result out to pinned
-    host memory, all inside the timed region.  The packed weights and scales
-    are the model's resident parameters (rotated over the same copies as the
-    device-timed loop, so they stream from HBM), not step inputs."""
+    """Same workload through the public API with the step's data in host
+    memory: every step calls nvfp4_linear_host (through its Python binding),
+    which copies the activations in from pinned host memory, runs the layer
+    and copies the result out to pinned host memory, all inside the timed
+    region.  The packed weights and scales are the model's resident
+    parameters (rotated over the same copies as the device-timed loop, so
+    they stream from HBM), not step inputs."""
     import torch
     hx = [x.cpu().pin_memory() for x in case.x]
     hy = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for y in case.y]
@@ -349,12 +350,10 @@ def e2e_case(case, steps, stream, dev):
 
     def one(i):
         c = i % case.copies
-        with torch.cuda.stream(stream):
-            for j, t in enumerate(case.linears):
-                dx[j].copy_(hx[j], non_blocking=True)
-                case.lib.linear_ex(dx[j], case.wp[c][j], case.ws[c][j], float(t.global_scale),
-                                   case.flags, out=case.y[j], stream=stream)
-                hy[j].copy_(case.y[j], non_blocking=True)
+        for j, t in enumerate(case.linears):
+            case.lib.linear_host(hx[j], dx[j], case.wp[c][j], case.ws[c][j],
+                                 float(t.global_scale), case.y[j], hy[j], case.flags,
+                                 stream=stream)
 
     for i in range(3):
         one(i)

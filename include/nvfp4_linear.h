@@ -189,6 +189,27 @@ int nvfp4_linear_ex(const void* x, const uint8_t* w_packed, const uint8_t* w_sca
                     float global_scale, void* y, int64_t M, int64_t N, int64_t K,
                     unsigned int flags, void* stream);
 
+/* nvfp4_linear_ex with the activations and the result in host memory:
+ * enqueues on `stream` a copy of x_host into the caller's device buffer
+ * x_dev, the layer (y_dev = x_dev . w^T as nvfp4_linear_ex), and a copy of
+ * y_dev into y_host -- one cudaMemcpyAsync each way around the launch;
+ * nothing is allocated.  (A convenience for callers whose activations live
+ * in host memory; the operation is that of nvfp4_linear_ex.)
+ *   x_host  host, bf16 [M, K] row-major;  x_dev  device, bf16 [M, K].
+ *   y_dev   device, the output of nvfp4_linear_ex for `flags` (bf16, or
+ *           fp32 with NVFP4_FLAG_F32_OUT; [M, N], or [M, N/2] with SWIGLU).
+ *   y_host  host, same shape and type as y_dev.
+ * For the copies to be asynchronous the host buffers must be page-locked
+ * (cudaHostAlloc / cudaHostRegister); pageable buffers work, but the copies
+ * then synchronise with the host.  The host buffers must stay valid, and
+ * x_host unchanged, until the stream has passed the copies.  Validation and
+ * errors as nvfp4_linear_ex (x_dev, y_dev in place of x, y; x_host and
+ * y_host must not be NULL when M > 0); NVFP4_ERR_LAUNCH also when a copy
+ * cannot be enqueued (an enqueued input copy is then left to complete). */
+int nvfp4_linear_host(const void* x_host, void* x_dev, const uint8_t* w_packed,
+                      const uint8_t* w_scale, float global_scale, void* y_dev, void* y_host,
+                      int64_t M, int64_t N, int64_t K, unsigned int flags, void* stream);
+
 /* Which kernel a call with these sizes and flags would launch
  * (NVFP4_KERNEL_*), or NVFP4_KERNEL_NONE if the call would be rejected.
  * Pure host function: touches no device. */

@@ -5,6 +5,7 @@ torch, the current CUDA stream, and the call.  Every step of the layer runs
 in the library's kernels; there is no CPU or PyTorch fallback, and a missing
 library or GPU raises.
 """
+import contextlib
 import ctypes
 import os
 import re
@@ -80,6 +81,8 @@ def load_library(path=None):
         f.argtypes = [P, P, P, ctypes.c_float, P, i64, i64, i64, P]
     lib.nvfp4_linear_ex.restype = ctypes.c_int
     lib.nvfp4_linear_ex.argtypes = [P, P, P, ctypes.c_float, P, i64, i64, i64, u32, P]
+    lib.nvfp4_linear_host.restype = ctypes.c_int
+    lib.nvfp4_linear_host.argtypes = [P, P, P, P, ctypes.c_float, P, P, i64, i64, i64, u32, P]
     lib.nvfp4_linear_swiglu_gs.restype = ctypes.c_int
     lib.nvfp4_linear_swiglu_gs.argtypes = [P, P, P, ctypes.c_float, ctypes.c_float, P, i64, i64,
                                            i64, u32, P]
@@ -149,6 +152,14 @@ def _check(x, w_packed, w_scale):
     return w_packed, w_scale, M, N, K
 
 
+def _on_device(device):
+    """Make `device` current for the call (the library works on the current
+    device); no switch, and no cost, when it already is."""
+    if device.index is None or device.index == torch.cuda.current_device():
+        return contextlib.nullcontext()
+    return torch.cuda.device(device)
+
+
 def linear_ex(x, w_packed, w_scale, global_scale, flags=0, out=None, stream=None):
     """Call nvfp4_linear_ex; allocate ``out`` if not given and return it."""
     w_packed, w_scale, M, N, K = _check(x, w_packed, w_scale)
@@ -162,13 +173,44 @@ def linear_ex(x, w_packed, w_scale, global_scale, flags=0, out=None, stream=None
                          % (dtype, (M, n_out), x.device))
     if stream is None:
         stream = torch.cuda.current_stream(x.device)
-    with torch.cuda.device(x.device):
+    with _on_device(x.device):
         st = library().nvfp4_linear_ex(x.data_ptr(), w_packed.data_ptr(), w_scale.data_ptr(),
                                        float(global_scale), out.data_ptr(), M, N, K,
                                        int(flags), ctypes.c_void_p(stream.cuda_stream))
     if st != OK:
         raise Nvfp4Error(st, "nvfp4_linear_ex")
     return out
+
+
+def linear_host(x_host, x_dev, w_packed, w_scale, global_scale, y_dev, y_host, flags=0,
+                stream=None):
+    """Call nvfp4_linear_host: copy the host activations ``x_host`` into the
+    device buffer ``x_dev``, run the layer into ``y_dev`` and copy it to the
+    host tensor ``y_host``, all enqueued on ``stream`` (page-locked host
+    tensors keep the copies asynchronous).  Returns ``y_host``."""
+    w_packed, w_scale, M, N, K = _check(x_dev, w_packed, w_scale)
+    n_out = N // 2 if flags & FLAG_SWIGLU else N
+    dtype = torch.float32 if flags & FLAG_F32_OUT else torch.bfloat16
+    for name, t, want_dev in (("x_host", x_host, False), ("y_host", y_host, False),
+                              ("y_dev", y_dev, True)):
+        shape = (M, K) if name == "x_host" else (M, n_out)
+        tdt = torch.bfloat16 if name == "x_host" else dtype
+        if (t.dtype != tdt or tuple(t.shape) != shape or not t.is_contiguous()
+                or t.is_cuda != want_dev or (want_dev and t.device != x_dev.device)):
+            raise ValueError("%s must be a contiguous %s tensor of shape %s %s"
+                             % (name, tdt, shape, "on %s" % x_dev.device if want_dev
+                                else "in host memory"))
+    if stream is None:
+        stream = torch.cuda.current_stream(x_dev.device)
+    with _on_device(x_dev.device):
+        st = library().nvfp4_linear_host(x_host.data_ptr(), x_dev.data_ptr(),
+                                         w_packed.data_ptr(), w_scale.data_ptr(),
+                                         float(global_scale), y_dev.data_ptr(),
+                                         y_host.data_ptr(), M, N, K, int(flags),
+                                         ctypes.c_void_p(stream.cuda_stream))
+    if st != OK:
+        raise Nvfp4Error(st, "nvfp4_linear_host")
+    return y_host
 
 
 def linear(x, w_packed, w_scale, global_scale, out=None, stream=None):
@@ -204,7 +246,7 @@ def linear_swiglu_gs(x, w_packed, w_scale, gate_global_scale, up_global_scale, f
                          % (dtype, (M, N // 2), x.device))
     if stream is None:
         stream = torch.cuda.current_stream(x.device)
-    with torch.cuda.device(x.device):
+    with _on_device(x.device):
         st = library().nvfp4_linear_swiglu_gs(
             x.data_ptr(), w_packed.data_ptr(), w_scale.data_ptr(), float(gate_global_scale),
             float(up_global_scale), out.data_ptr(), M, N, K, int(flags),
@@ -231,7 +273,7 @@ def linear_segmented(x, w_packed, w_scale, global_scales, segment_rows, flags=0,
                          % (dtype, (M, N), x.device))
     if stream is None:
         stream = torch.cuda.current_stream(x.device)
-    with torch.cuda.device(x.device):
+    with _on_device(x.device):
         st = library().nvfp4_linear_segmented(
             x.data_ptr(), w_packed.data_ptr(), w_scale.data_ptr(), ctypes.cast(gs, ctypes.c_void_p),
             ctypes.cast(rows, ctypes.c_void_p), len(segment_rows), out.data_ptr(), M, N, K,
@@ -254,7 +296,7 @@ def quantize(w, stream=None):
     gs = torch.empty(1, dtype=torch.float32, device=w.device)
     if stream is None:
         stream = torch.cuda.current_stream(w.device)
-    with torch.cuda.device(w.device):
+    with _on_device(w.device):
         st = library().nvfp4_quantize(w.data_ptr(), N, K, wp.data_ptr(), ws.data_ptr(),
                                       gs.data_ptr(), ctypes.c_void_p(stream.cuda_stream))
     if st != OK:

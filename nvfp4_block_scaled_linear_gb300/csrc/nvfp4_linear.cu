@@ -329,6 +329,54 @@ int kernel_for(int64_t M, int64_t N, int64_t K, unsigned int flags) {
   return NVFP4_KERNEL_SMALLM;
 }
 
+// Plans depend only on the device and (M, N, K, flags), and the search
+// over CTA shapes costs microseconds of host time per call -- as much as a
+// decode-sized kernel's launch -- so each planner keeps its results in a
+// small direct-mapped cache (a miss recomputes; a hit is always valid, the
+// key holding every input of the search).
+template <typename Plan>
+class PlanMemo {
+ public:
+  template <typename Fn>
+  Plan get(const DeviceInfo& d, int64_t M, int64_t N, int64_t K, unsigned int flags, Fn&& make) {
+    const Key key{&d, M, N, K, flags};
+    uint64_t h = static_cast<uint64_t>(M) * 0x9E3779B97F4A7C15ull ^
+                 static_cast<uint64_t>(N) * 0xC2B2AE3D27D4EB4Full ^
+                 static_cast<uint64_t>(K) * 0x165667B19E3779F9ull ^ (uint64_t(flags) << 1) ^
+                 (reinterpret_cast<uintptr_t>(&d) >> 4);
+    h ^= h >> 31;
+    Slot& slot = slots_[h % kSlots];
+    {
+      std::lock_guard<std::mutex> lock(mu_);
+      if (slot.valid && slot.key == key) return slot.plan;
+    }
+    const Plan plan = make();
+    std::lock_guard<std::mutex> lock(mu_);
+    slot.valid = true;
+    slot.key = key;
+    slot.plan = plan;
+    return plan;
+  }
+
+ private:
+  struct Key {
+    const DeviceInfo* dev;
+    int64_t M, N, K;
+    unsigned int flags;
+    bool operator==(const Key& o) const {
+      return dev == o.dev && M == o.M && N == o.N && K == o.K && flags == o.flags;
+    }
+  };
+  struct Slot {
+    bool valid = false;
+    Key key{};
+    Plan plan{};
+  };
+  static constexpr int kSlots = 64;
+  Slot slots_[kSlots];
+  std::mutex mu_;
+};
+
 struct SmallmPlan {
   int groups = 0;
   int split = 0;
@@ -405,7 +453,9 @@ int launch_smallm(const DeviceInfo& d, const void* x, const uint8_t* wp, const u
                   float gs, float gs_up, void* y, int64_t M, int64_t N, int64_t K, unsigned int flags,
                   cudaStream_t stream, const SegSpec* segs) {
   const bool swiglu = flags & NVFP4_FLAG_SWIGLU;
-  const SmallmPlan plan = plan_smallm<MT, F16>(d, M, N, K, flags);
+  static PlanMemo<SmallmPlan> memo;
+  const SmallmPlan plan =
+      memo.get(d, M, N, K, flags, [&] { return plan_smallm<MT, F16>(d, M, N, K, flags); });
   if (plan.groups == 0) return NVFP4_ERR_INVALID;   // overrides that cannot run
   const int half_rows = 8 * plan.groups;
   CUtensorMap tw, ts, tx;
@@ -523,7 +573,9 @@ template <int NM>
 int launch_gemv(const DeviceInfo& d, const void* x, const uint8_t* wp, const uint8_t* ws,
                 float gs, float gs_up, void* y, int64_t M, int64_t N, int64_t K, unsigned int flags,
                 cudaStream_t stream, const SegSpec* segs) {
-  const GemvPlan plan = plan_gemv<NM>(d, M, N, K, flags);
+  static PlanMemo<GemvPlan> memo;
+  const GemvPlan plan =
+      memo.get(d, M, N, K, flags, [&] { return plan_gemv<NM>(d, M, N, K, flags); });
   if (plan.stages == 0) return NVFP4_ERR_INVALID;   // an override that cannot run
   CUtensorMap tw, ts, tx;
   if (!encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, wp, K / 2, N, K / 2, 128, gt::kHalfRows,
@@ -624,7 +676,9 @@ template <int NM, int NI>
 int launch_gemv_bf16(const DeviceInfo& d, const void* x, const uint8_t* wp, const uint8_t* ws,
                      float gs, float gs_up, void* y, int64_t M, int64_t N, int64_t K,
                      unsigned int flags, cudaStream_t stream, const SegSpec* segs) {
-  const GemvBfPlan plan = plan_gemv_bf16<NM, NI>(d, N, K, flags);
+  static PlanMemo<GemvBfPlan> memo;
+  const GemvBfPlan plan =
+      memo.get(d, 0, N, K, flags, [&] { return plan_gemv_bf16<NM, NI>(d, N, K, flags); });
   if (plan.stages == 0) return NVFP4_ERR_INVALID;   // an override that cannot run
   CUtensorMap tw, ts, tx;
   if (!encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, wp, K / 2, N, K / 2, 128, gb::kHalfRows,
@@ -815,6 +869,32 @@ int nvfp4_linear_ex(const void* x, const uint8_t* w_packed, const uint8_t* w_sca
                     float global_scale, void* y, int64_t M, int64_t N, int64_t K,
                     unsigned int flags, void* stream) {
   return run(x, w_packed, w_scale, global_scale, global_scale, y, M, N, K, flags, stream);
+}
+
+int nvfp4_linear_host(const void* x_host, void* x_dev, const uint8_t* w_packed,
+                      const uint8_t* w_scale, float global_scale, void* y_dev, void* y_host,
+                      int64_t M, int64_t N, int64_t K, unsigned int flags, void* stream_ptr) {
+  int st = validate(x_dev, w_packed, w_scale, y_dev, M, N, K, flags);
+  if (st != NVFP4_OK) return st;
+  if (M == 0) return NVFP4_OK;
+  if (!x_host || !y_host) return NVFP4_ERR_INVALID;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  const size_t x_bytes = static_cast<size_t>(M) * static_cast<size_t>(K) * 2;
+  const int64_t n_out = (flags & NVFP4_FLAG_SWIGLU) ? N / 2 : N;
+  const size_t y_bytes = static_cast<size_t>(M) * static_cast<size_t>(n_out) *
+                         ((flags & NVFP4_FLAG_F32_OUT) ? 4 : 2);
+  if (cudaMemcpyAsync(x_dev, x_host, x_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return NVFP4_ERR_LAUNCH;
+  }
+  st = run(x_dev, w_packed, w_scale, global_scale, global_scale, y_dev, M, N, K, flags,
+           stream_ptr);
+  if (st != NVFP4_OK) return st;
+  if (cudaMemcpyAsync(y_host, y_dev, y_bytes, cudaMemcpyDeviceToHost, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return NVFP4_ERR_LAUNCH;
+  }
+  return NVFP4_OK;
 }
 
 int nvfp4_linear_swiglu_gs(const void* x, const uint8_t* w_packed, const uint8_t* w_scale,

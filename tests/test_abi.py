@@ -139,6 +139,14 @@ def test_rejects_before_any_device_work(lib):
     assert q(A, 4, 40, A, A, F, None) == -3                  # K % 16
     assert q(A + 8, 4, 64, A, A, F, None) == -2               # w not 16-byte aligned
     assert q(A, 4, 64, A + 4, A, F, None) == -2               # codes not 8-byte aligned
+    h = lib.nvfp4_linear_host
+    H = 0x30000            # fake host address, never dereferenced
+    assert h(None, A, A, A, ctypes.c_float(1.0), A, H, 1, 256, 512, 0, None) == -1
+    assert h(H, A, A, A, ctypes.c_float(1.0), A, None, 1, 256, 512, 0, None) == -1
+    assert h(H, None, A, A, ctypes.c_float(1.0), A, H, 1, 256, 512, 0, None) == -1
+    assert h(H, A, A, A, ctypes.c_float(1.0), A + 2, H, 1, 256, 512, 0, None) == -2
+    assert h(H, A, A, A, ctypes.c_float(1.0), A, H, 1, 256, 384, 0, None) == -3
+    assert h(None, None, A, A, ctypes.c_float(1.0), None, None, 0, 256, 512, 0, None) == 0
     # tuning overrides out of range
     assert lib.nvfp4_linear_ex(A, A, A, ctypes.c_float(1.0), A, 1, 256, 512,
                                _lib.FLAG_SPLIT(17), None) == -1

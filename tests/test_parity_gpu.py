@@ -470,6 +470,61 @@ def test_repeated_calls_are_deterministic():
         assert np.array_equal(bf16_bits(run(t)), a)
 
 
+def test_concurrent_calls_from_two_threads_on_two_streams():
+    """Every call shares the library's host state (device set-up, plan and
+    descriptor caches): two threads calling at once, each on its own
+    stream, with shapes that take different kernels and plans, get the
+    outputs of calls made one at a time, bit for bit."""
+    import threading
+    cases = [(make_linear(1, 1024, 2048, seed=3000), 0),
+             (make_linear(20, 768, 1024, seed=3001), 0),
+             (make_linear(12, 512, 2048, seed=3002), GEMV_BF16 | _lib.FLAG_SPLIT(2)),
+             (make_linear(5, 640, 1024, seed=3003), _lib.FLAG_SWIGLU)]
+    refs = [bf16_bits(run(t, fl)) for t, fl in cases]
+    failures = []
+
+    def worker(items):
+        s = torch.cuda.Stream()
+        dev = [(to_dev(t), t, fl, ref) for (t, fl), ref in items]
+        for i in range(40):
+            for (x, wp, ws), t, fl, ref in dev:
+                y = _lib.linear_ex(x, wp, ws, float(t.global_scale), fl, stream=s)
+                s.synchronize()
+                if not np.array_equal(bf16_bits(y), ref):
+                    failures.append((t.M, fl, i))
+                    return
+
+    pairs = list(zip(cases, refs))
+    threads = [threading.Thread(target=worker, args=(pairs[k::2],)) for k in range(2)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not failures, failures
+
+
+@pytest.mark.parametrize("M,flags,pinned", [(1, 0, True), (7, _lib.FLAG_SWIGLU, True),
+                                            (20, _lib.FLAG_F32_OUT, False), (40, 0, True)])
+def test_host_buffer_call_equals_device_call(M, flags, pinned):
+    """nvfp4_linear_host (activations and result in host memory, page-locked
+    or not) gives the device call's output bit for bit."""
+    t = make_linear(M, 512, 1024, seed=3100 + M)
+    x, wp, ws = to_dev(t)
+    ref = _lib.linear_ex(x, wp, ws, float(t.global_scale), flags).cpu()
+    hx = x.cpu()
+    hy = torch.empty(ref.shape, dtype=ref.dtype)
+    if pinned:
+        hx, hy = hx.pin_memory(), hy.pin_memory()
+    dx = torch.empty_like(x)
+    dy = torch.empty(ref.shape, dtype=ref.dtype, device=x.device)
+    s = torch.cuda.Stream()
+    _lib.linear_host(hx, dx, wp, ws, float(t.global_scale), dy, hy, flags, stream=s)
+    s.synchronize()
+    assert torch.equal(hy.view(torch.int16) if hy.dtype == torch.bfloat16 else hy,
+                       ref.view(torch.int16) if ref.dtype == torch.bfloat16 else ref)
+    assert torch.equal(dx.cpu().view(torch.int16), x.cpu().view(torch.int16))
+
+
 def test_cuda_graph_capture_and_replay():
     """Calls captured into a CUDA graph (both kernels, SwiGLU and plain)
     give on replay what the same calls give eagerly, bit for bit, also after
