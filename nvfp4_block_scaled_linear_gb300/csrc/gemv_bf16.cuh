@@ -426,11 +426,9 @@ __global__ void __launch_bounds__(Roles<NM, NI>::kThreads, Roles<NM, NI>::kCtasP
         v = part[jr * NM + m];
         if (p.swiglu) u = part[(kHalfRows + jr) * NM + m];
       } else {
-        for (int c = 0; c < split; ++c) {
-          const uint32_t base = map_to_rank(part_local, c);
-          v += ld_cluster_f32(base + 4u * (jr * NM + m));
-          if (p.swiglu) u += ld_cluster_f32(base + 4u * ((kHalfRows + jr) * NM + m));
-        }
+        v = cluster_sum_f32<kMaxSplit>(part_local, 4u * (jr * NM + m), split);
+        if (p.swiglu)
+          u = cluster_sum_f32<kMaxSplit>(part_local, 4u * ((kHalfRows + jr) * NM + m), split);
       }
       float yv = v * (p.seg.n ? seg_scale(p.seg, n_base + jr) : p.out_scale);
       if (p.swiglu) yv = silu_mul(yv, u * p.out_scale_up);

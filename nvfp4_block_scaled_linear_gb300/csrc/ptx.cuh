@@ -162,6 +162,24 @@ __device__ __forceinline__ float ld_cluster_f32(uint32_t cluster_addr) {
   return v;
 }
 
+// Sum, in rank order, of the float at byte offset `off` of the
+// shared-memory object at `local` over CTAs 0..n-1 of the cluster (n <=
+// kMax).  Every remote load is issued before the first add, so that their
+// latencies overlap (one add after each load had left the warp waiting out
+// each remote load in turn).
+template <int kMax>
+__device__ __forceinline__ float cluster_sum_f32(uint32_t local, uint32_t off, int n) {
+  float v[kMax];
+#pragma unroll
+  for (int q = 0; q < kMax; ++q)
+    if (q < n) v[q] = ld_cluster_f32(map_to_rank(local, static_cast<uint32_t>(q)) + off);
+  float s = 0.f;
+#pragma unroll
+  for (int q = 0; q < kMax; ++q)
+    if (q < n) s += v[q];
+  return s;
+}
+
 // ---------------------------------------------------------------- bf16 math
 __device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
   uint32_t d;

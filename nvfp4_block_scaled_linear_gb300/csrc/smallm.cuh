@@ -516,11 +516,9 @@ __global__ void __launch_bounds__(threads_for(F16), F16 ? 2 : 1)
         v = part[j * C + m];
         if (p.swiglu) u = part[(half_rows + j) * C + m];
       } else {
-        for (int q = 0; q < split; ++q) {
-          const uint32_t base = map_to_rank(part_local, q);
-          v += ld_cluster_f32(base + 4u * (j * C + m));
-          if (p.swiglu) u += ld_cluster_f32(base + 4u * ((half_rows + j) * C + m));
-        }
+        v = cluster_sum_f32<kMaxSplit>(part_local, 4u * (j * C + m), split);
+        if (p.swiglu)
+          u = cluster_sum_f32<kMaxSplit>(part_local, 4u * ((half_rows + j) * C + m), split);
       }
       float yv = v * (p.seg.n ? seg_scale(p.seg, n_base + j) : p.out_scale);
       if (p.swiglu) yv = silu_mul(yv, u * p.out_scale_up);
