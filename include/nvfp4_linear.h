@@ -27,8 +27,9 @@
  * Ownership: every buffer belongs to the caller.  The library allocates no
  * device or host memory per call and keeps no state besides per-device
  * attributes it caches on first use (device properties, kernel attributes,
- * the address of its device error word) and a small cache of encoded TMA
- * descriptors, keyed by every input of the encoding (pointer, sizes, box).
+ * the address of its device error word) and small caches of encoded TMA
+ * descriptors, keyed by every input of the encoding (pointer, sizes, box),
+ * and of launch plans, keyed by device, M, N, K and flags.
  *
  * Behaviour: calls are asynchronous on `stream`; they validate on the host,
  * launch one kernel, and return without synchronising.  A rejected call
