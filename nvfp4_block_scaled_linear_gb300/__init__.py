@@ -9,11 +9,11 @@ from .inputs import WORKLOADS, LinearInputs, algorithmic_bytes, flops  # noqa: F
 
 
 def __getattr__(name):
-    # The binding is imported lazily so that the input generators stay
+    # The binding (every public name of _lib: the calls, the flag and kernel
+    # constants) is imported lazily so that the input generators stay
     # importable on machines without the built library.
-    if name in ("linear", "linear_f32", "linear_swiglu", "linear_swiglu_f32",
-                "status_string", "abi_version", "device_error", "library",
-                "Nvfp4Error", "load_library", "choose_plan"):
+    if not name.startswith("_"):
         from . import _lib
-        return getattr(_lib, name)
+        if hasattr(_lib, name):
+            return getattr(_lib, name)
     raise AttributeError(name)
