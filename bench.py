@@ -507,14 +507,9 @@ def _oracle_step(t, rows, threads):
                              threads=threads)
 
 
-def cpu_baseline(case, budget_s=10.0):
-    """The oracle, as it stands, on the host cores: repeated passes over a
-    row sample of the headline workload for about budget_s seconds."""
-    import oracle
-    from nvfp4_block_scaled_linear_gb300.inputs import algorithmic_bytes
-    threads = oracle.default_threads()
-    t = case.linears[0]
-    # size one pass at ~1 s
+def _oracle_rate(t, threads, budget_s):
+    """(GB/s, passes, rows, seconds) of the oracle on `threads` threads:
+    repeated passes over a row sample sized at ~1 s per pass."""
     rows = slice(0, min(t.N, 2048))
     t0 = time.time()
     _oracle_step(t, rows, threads)
@@ -528,10 +523,46 @@ def cpu_baseline(case, budget_s=10.0):
     el = time.time() - t0
     frac = n_rows / t.N
     byts = (t.N * t.K // 2 + t.N * t.K // 16) * frac + 2 * t.M * t.K + 2 * t.M * n_rows
-    return {"value": round(byts * done / el / 1e9, 4), "unit": "GB/s", "cores": threads,
+    return byts * done / el / 1e9, done, n_rows, el
+
+
+def _cpu_model():
+    import subprocess
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=5).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":")[0].strip().lower()
+                if key in ("model name", "cpu model", "hardware"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def cpu_baseline(case, budget_s=10.0):
+    """The oracle, as it stands, on the host cores (all of them, and one):
+    repeated passes over a row sample of the headline workload for about
+    budget_s (and budget_s / 3) seconds."""
+    import oracle
+    threads = oracle.default_threads()
+    t = case.linears[0]
+    value, done, n_rows, el = _oracle_rate(t, threads, budget_s)
+    value1, done1, n_rows1, el1 = _oracle_rate(t, 1, budget_s / 3.0)
+    return {"value": round(value, 4), "unit": "GB/s", "cores": threads,
             "kind": "oracle",
             "sample": "%d passes over rows [0,%d) of %s (M=%d K=%d), %.1f s" % (
-                done, n_rows, case.name, t.M, t.K, el)}
+                done, n_rows, case.name, t.M, t.K, el),
+            "one_core": {"value": round(value1, 4), "sample": "%d passes over rows [0,%d), %.1f s"
+                         % (done1, n_rows1, el1)},
+            "cpu": _cpu_model()}
 
 
 def run_reference(args):

@@ -63,6 +63,8 @@ def _load():
     lib.oracle_e2m1_round.argtypes = [ctypes.c_float]
     lib.oracle_quantize.restype = ctypes.c_int
     lib.oracle_quantize.argtypes = [P, i64, i64, P, P, P]
+    lib.oracle_fp8_to_bf16.restype = ctypes.c_int
+    lib.oracle_fp8_to_bf16.argtypes = [P, P, i64, i64, i64, P]
     _lib = lib
     return lib
 
@@ -194,3 +196,24 @@ def quantize(w_bits):
     if _load().oracle_quantize(_ptr(w_bits), N, K, _ptr(wp), _ptr(ws), _ptr(gs)) != 0:
         raise ValueError("bad shape for the quantiser: %s" % (w_bits.shape,))
     return wp, ws, np.float32(gs[0])
+
+
+def fp8_to_bf16(w8, scale_inv, block=128):
+    """Block-scaled FP8 e4m3 [N, K] (bits) with fp32 scale_inv [ceil(N/B),
+    ceil(K/B)] -> bf16 bits [N, K]: RNE_bf16(fp32(e4m3 * scale_inv)), per
+    nvfp4_oracle.c."""
+    w8 = np.ascontiguousarray(w8, np.uint8)
+    N, K = w8.shape
+    sinv = np.ascontiguousarray(scale_inv, np.float32)
+    if sinv.shape != (-(-N // block), -(-K // block)):
+        raise ValueError("scale_inv must be [ceil(N/%d), ceil(K/%d)]" % (block, block))
+    out = np.zeros((N, K), np.uint16)
+    if _load().oracle_fp8_to_bf16(_ptr(w8), _ptr(sinv), block, N, K, _ptr(out)) != 0:
+        raise ValueError("bad shape")
+    return out
+
+
+def quantize_fp8(w8, scale_inv, block=128):
+    """FP8 -> BF16 -> NVFP4: fp8_to_bf16, then quantize."""
+    return quantize(fp8_to_bf16(w8, scale_inv, block))
+

@@ -369,3 +369,26 @@ int oracle_quantize(const uint16_t* w_bits, int64_t N, int64_t K, uint8_t* w_pac
     }
     return 0;
 }
+
+/* A block-scaled FP8 checkpoint tensor as bf16: the first step of the
+ * FP8 -> BF16 -> NVFP4 conversion the pages describe for FP8-source weights
+ * (FlashRT docs, "Qwen3.6-27B NVFP4 on RTX 5090", the MTP-head note: FP8
+ * e4m3 in blocks of 128 converted once at load; qwentin README, "Convert a
+ * model": block-scaled E4M3 tensors with `*_scale_inv` are dequantised
+ * first).  w8: e4m3fn bits [N][K]; scale_inv: fp32 [ceil(N/B)][ceil(K/B)];
+ * out: bf16 bits [N][K], each RNE_bf16(fp32(e4m3(w8) * scale_inv of its
+ * B x B block)).  Returns 0, or -1 on a bad shape. */
+int oracle_fp8_to_bf16(const uint8_t* w8, const float* scale_inv, int64_t block, int64_t N,
+                       int64_t K, uint16_t* out)
+{
+    if (N <= 0 || K <= 0 || block <= 0) return -1;
+    const int64_t kb = (K + block - 1) / block;
+    for (int64_t n = 0; n < N; ++n) {
+        for (int64_t k = 0; k < K; ++k) {
+            const float v = (float)oracle_e4m3(w8[n * K + k]);   /* exact in fp32 */
+            const float p = v * scale_inv[(n / block) * kb + k / block];
+            out[n * K + k] = oracle_f32_to_bf16_rne(p);
+        }
+    }
+    return 0;
+}

@@ -46,6 +46,12 @@ MUTANTS = {
                             "if (d < best_d || (d == best_d && (b & 1u) == 1)) {"),
     "quant_codes_use_unrounded_scale": ("const float s = (float)oracle_e4m3(sbyte);",
                                         "const float s = s_f;"),
+    "fp8_scale_divides": ("const float p = v * scale_inv[(n / block) * kb + k / block];",
+                          "const float p = v / scale_inv[(n / block) * kb + k / block];"),
+    "fp8_row_blocks_ignored": ("const float p = v * scale_inv[(n / block) * kb + k / block];",
+                               "const float p = v * scale_inv[k / block];"),
+    "fp8_scale_dropped": ("const float p = v * scale_inv[(n / block) * kb + k / block];",
+                          "const float p = v;"),
     "quant_nibbles_swapped": ("w_packed[n * (K / 2) + b * 8 + j / 2] = (uint8_t)(c[0] | (c[1] << 4));",
                               "w_packed[n * (K / 2) + b * 8 + j / 2] = (uint8_t)(c[1] | (c[0] << 4));"),
 }
@@ -71,7 +77,25 @@ def _build(tmp_path, name, source):
     lib.oracle_e2m1_round.argtypes = [ctypes.c_float]
     lib.oracle_e4m3_round.restype = ctypes.c_uint
     lib.oracle_e4m3_round.argtypes = [ctypes.c_float]
+    lib.oracle_fp8_to_bf16.restype = ctypes.c_int
+    lib.oracle_fp8_to_bf16.argtypes = [P, P, i64, i64, i64, P]
     return lib
+
+
+def fp8_torch_case(N=200, K=272, block=128, seed=5):
+    """A ragged block-scaled FP8 tensor with distinct non-power-of-two
+    scales per block, and its bf16 image by torch's own e4m3 decode, fp32
+    multiply and bf16 rounding."""
+    rng = np.random.default_rng(seed)
+    w8 = rng.integers(0, 256, size=(N, K), dtype=np.uint8)
+    w8[(w8 & 0x7F) == 0x7F] = 0x3A                     # no NaN codes
+    nb, kb = -(-N // block), -(-K // block)
+    sinv = np.exp(rng.uniform(-6, 6, size=(nb, kb))).astype(np.float32)
+    x = torch.from_numpy(w8).view(torch.float8_e4m3fn).to(torch.float32)
+    s_full = torch.from_numpy(sinv).repeat_interleave(block, 0)[:N] \
+        .repeat_interleave(block, 1)[:, :K]
+    want = (x * s_full).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    return w8, sinv, want
 
 
 def _p(a):
@@ -123,6 +147,11 @@ def _pins_pass(lib) -> bool:
     ev = np.float32([9.5, 10.5, 0.0546875, 1.0 + 1.0 / 16, 448.0])
     want = torch.from_numpy(ev).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
     if [lib.oracle_e4m3_round(float(v)) for v in ev] != list(want):
+        return False
+    w8, sinv, want = fp8_torch_case()
+    got = np.zeros(w8.shape, np.uint16)
+    lib.oracle_fp8_to_bf16(_p(w8), _p(sinv), 128, w8.shape[0], w8.shape[1], _p(got))
+    if not np.array_equal(got, want):
         return False
     for case in json.load(open(os.path.join(GOLDEN, "quantize_blocks.json")))["cases"]:
         w = torch.tensor(case["w"], dtype=torch.float32).to(torch.bfloat16) \
