@@ -395,6 +395,34 @@ def quantize_case(lib, dev, stream, hbm_peak, N=34816, K=5120, steps=20):
             "GB/s": round(gbs, 1), "frac_hbm_peak": round(gbs / hbm_peak, 4)}
 
 
+def quantize_fp8_case(lib, dev, stream, hbm_peak, N=34816, K=5120, block=128, steps=20):
+    """The load-time FP8 -> NVFP4 conversion on the same weight shape:
+    bytes = e4m3 codes and block scales in + codes + scales out."""
+    import torch
+    g = torch.Generator(device="cpu").manual_seed(12)
+    w8 = (torch.randn((N, K), generator=g) * 60.0).to(torch.float8_e4m3fn).to(dev)
+    sinv = torch.exp(torch.empty((-(-N // block), -(-K // block))).uniform_(-9, 2, generator=g)) \
+        .to(dev)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            lib.quantize_fp8(w8, sinv, block, stream=stream)
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(steps):
+            lib.quantize_fp8(w8, sinv, block, stream=stream)
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    nbytes = N * K + sinv.numel() * 4 + N * K // 2 + N * K // 16 + 4
+    gbs = nbytes / (ms / 1e3) / 1e9
+    del w8, sinv
+    return {"ms_per_step": round(ms, 5), "kernel": "quantize_fp8", "shape": [N, K],
+            "block": block, "GB/s": round(gbs, 1), "frac_hbm_peak": round(gbs / hbm_peak, 4)}
+
+
 def run_ours(args):
     import torch
     from nvfp4_block_scaled_linear_gb300 import build as cuda_build
@@ -487,6 +515,7 @@ def run_ours(args):
                                  graph=False)
             line["eager_ms_per_step"] = round(e_tot / min(args.steps, 500), 6)
         extras["quantize"] = quantize_case(lib, dev, stream, hbm_peak)
+        extras["quantize_fp8"] = quantize_fp8_case(lib, dev, stream, hbm_peak)
         line["workloads"] = extras
         line["gpu_launches_extras"] = "not in the headline timed region"
     sampler.stop()

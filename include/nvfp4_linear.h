@@ -183,6 +183,26 @@ int nvfp4_linear_segmented(const void* x, const uint8_t* w_packed, const uint8_t
 int nvfp4_quantize(const void* w, int64_t N, int64_t K, uint8_t* w_packed, uint8_t* w_scale,
                    float* global_scale, void* stream);
 
+/* nvfp4_quantize for a block-scaled FP8 checkpoint tensor: the FP8 -> BF16
+ * -> NVFP4 conversion (FlashRT docs, "Qwen3.6-27B NVFP4 on RTX 5090", the
+ * MTP-head note: FP8 e4m3 in blocks of 128, converted FP8 -> BF16 -> NVFP4
+ * once at load; qwentin README, "Convert a model": block-scaled E4M3
+ * tensors with `*_scale_inv` are dequantised first).
+ *   w_fp8      device, uint8 [N, K]: e4m3fn bits, row-major; 16-byte aligned.
+ *   scale_inv  device, fp32 [ceil(N/block), ceil(K/block)], row-major: the
+ *              factor of every weight of its block x block tile.
+ *   block      the tile edge (128 in the checkpoints above), a multiple of 16.
+ * Each weight's bf16 image is RNE_bf16(fp32(e4m3 * scale_inv)); the outputs
+ * are then exactly those of nvfp4_quantize on that bf16 tensor (which is
+ * never stored: both passes form it on the fly).  K % 16 == 0.  NaN codes
+ * (S.1111.111) are outside this contract.  Asynchronous on `stream` (a
+ * memset and three kernels); allocates nothing.  Errors: NVFP4_ERR_INVALID
+ * (NULL, sizes <= 0), NVFP4_ERR_MISALIGNED, NVFP4_ERR_SHAPE (K or block not
+ * a multiple of 16), NVFP4_ERR_LAUNCH, NVFP4_ERR_DEVICE. */
+int nvfp4_quantize_fp8(const uint8_t* w_fp8, const float* scale_inv, int64_t block, int64_t N,
+                       int64_t K, uint8_t* w_packed, uint8_t* w_scale, float* global_scale,
+                       void* stream);
+
 /* General form of the four calls above; `flags` is an OR of NVFP4_FLAG_*.
  * The FORCE flags pick a kernel regardless of M (for A/B measurements and
  * for checking both kernels on the same inputs). */

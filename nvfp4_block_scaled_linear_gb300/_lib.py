@@ -90,6 +90,8 @@ def load_library(path=None):
     lib.nvfp4_linear_segmented.argtypes = [P, P, P, P, P, ctypes.c_int, P, i64, i64, i64, u32, P]
     lib.nvfp4_quantize.restype = ctypes.c_int
     lib.nvfp4_quantize.argtypes = [P, i64, i64, P, P, P, P]
+    lib.nvfp4_quantize_fp8.restype = ctypes.c_int
+    lib.nvfp4_quantize_fp8.argtypes = [P, P, i64, i64, i64, P, P, P, P]
     lib.nvfp4_linear_kernel_for.restype = ctypes.c_int
     lib.nvfp4_linear_kernel_for.argtypes = [i64, i64, i64, u32]
     lib.nvfp4_device_status.restype = ctypes.c_int
@@ -301,6 +303,35 @@ def quantize(w, stream=None):
                                       gs.data_ptr(), ctypes.c_void_p(stream.cuda_stream))
     if st != OK:
         raise Nvfp4Error(st, "nvfp4_quantize")
+    return wp, ws, gs
+
+
+def quantize_fp8(w_fp8, scale_inv, block=128, stream=None):
+    """nvfp4_quantize_fp8: a block-scaled FP8 tensor (e4m3 [N, K], as uint8
+    or float8_e4m3fn, with fp32 scale_inv [ceil(N/block), ceil(K/block)])
+    -> (w_packed, w_scale, global_scale) like ``quantize``."""
+    if not (w_fp8.is_cuda and scale_inv.is_cuda) or w_fp8.device != scale_inv.device:
+        raise ValueError("w_fp8 and scale_inv must be CUDA tensors on one device")
+    if w_fp8.dtype == torch.float8_e4m3fn:
+        w_fp8 = w_fp8.view(torch.uint8)
+    if w_fp8.dtype != torch.uint8 or w_fp8.dim() != 2 or not w_fp8.is_contiguous():
+        raise TypeError("w_fp8 must be a contiguous 2-D uint8 / float8_e4m3fn tensor")
+    N, K = w_fp8.shape
+    shape = (-(-N // block), -(-K // block))
+    if (scale_inv.dtype != torch.float32 or tuple(scale_inv.shape) != shape
+            or not scale_inv.is_contiguous()):
+        raise ValueError("scale_inv must be a contiguous float32 tensor of shape %s" % (shape,))
+    wp = torch.empty((N, K // 2), dtype=torch.uint8, device=w_fp8.device)
+    ws = torch.empty((N, K // 16), dtype=torch.uint8, device=w_fp8.device)
+    gs = torch.empty(1, dtype=torch.float32, device=w_fp8.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(w_fp8.device)
+    with _on_device(w_fp8.device):
+        st = library().nvfp4_quantize_fp8(w_fp8.data_ptr(), scale_inv.data_ptr(), int(block),
+                                          N, K, wp.data_ptr(), ws.data_ptr(), gs.data_ptr(),
+                                          ctypes.c_void_p(stream.cuda_stream))
+    if st != OK:
+        raise Nvfp4Error(st, "nvfp4_quantize_fp8")
     return wp, ws, gs
 
 

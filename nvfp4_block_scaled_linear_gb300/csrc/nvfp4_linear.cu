@@ -959,6 +959,45 @@ int nvfp4_quantize(const void* w, int64_t N, int64_t K, uint8_t* w_packed, uint8
   return NVFP4_OK;
 }
 
+int nvfp4_quantize_fp8(const uint8_t* w_fp8, const float* scale_inv, int64_t block, int64_t N,
+                       int64_t K, uint8_t* w_packed, uint8_t* w_scale, float* global_scale,
+                       void* stream_ptr) {
+  namespace Q = nvfp4::quant;
+  if (!w_fp8 || !scale_inv || !w_packed || !w_scale || !global_scale || N <= 0 || K <= 0 ||
+      block <= 0)
+    return NVFP4_ERR_INVALID;
+  if ((reinterpret_cast<uintptr_t>(w_fp8) & 15u) || (reinterpret_cast<uintptr_t>(w_packed) & 7u) ||
+      (reinterpret_cast<uintptr_t>(scale_inv) & 3u) ||
+      (reinterpret_cast<uintptr_t>(global_scale) & 3u))
+    return NVFP4_ERR_MISALIGNED;
+  if (K % 16 != 0 || block % 16 != 0 || N > (int64_t(1) << 31) || K > (int64_t(1) << 31))
+    return NVFP4_ERR_SHAPE;
+  DeviceInfo* d = nullptr;
+  const int st = device_setup(&d);
+  if (st != NVFP4_OK) return st;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  Q::Fp8Layout L;
+  L.n_blocks = N * (K / 16);
+  L.k_blocks = K / 16;
+  L.kb = (K + block - 1) / block;
+  L.B = block;
+  const int64_t grid_cap = static_cast<int64_t>(d->num_sms) * 8;
+  const unsigned grid = static_cast<unsigned>(
+      std::min<int64_t>(grid_cap, (L.n_blocks + Q::kThreads - 1) / Q::kThreads));
+  unsigned int* amax_bits = reinterpret_cast<unsigned int*>(global_scale);
+  if (cudaMemsetAsync(global_scale, 0, sizeof(float), stream) != cudaSuccess) {
+    cudaGetLastError();
+    return NVFP4_ERR_LAUNCH;
+  }
+  const uint4* w = reinterpret_cast<const uint4*>(w_fp8);
+  Q::amax_fp8_kernel<<<grid, Q::kThreads, 0, stream>>>(w, scale_inv, L, amax_bits);
+  Q::quantize_fp8_kernel<<<grid, Q::kThreads, 0, stream>>>(
+      w, scale_inv, L, amax_bits, reinterpret_cast<uint2*>(w_packed), w_scale);
+  Q::finalize_kernel<<<1, 32, 0, stream>>>(global_scale);
+  if (cudaGetLastError() != cudaSuccess) return NVFP4_ERR_LAUNCH;
+  return NVFP4_OK;
+}
+
 int nvfp4_linear_kernel_for(int64_t M, int64_t N, int64_t K, unsigned int flags) {
   static const uint8_t dummy[16] __attribute__((aligned(16))) = {0};
   if (validate(dummy, dummy, dummy, dummy, M, N, K, flags) != NVFP4_OK || M == 0)

@@ -28,6 +28,8 @@
 // significands in the tests).
 #pragma once
 #include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "ptx.cuh"
 
@@ -107,6 +109,30 @@ __device__ __forceinline__ uint32_t to_e2m1x2(float lo, float hi) {
   return d;
 }
 
+// One 16-input block: its 16 weights (fp32 values of bf16 numbers) -> the
+// block's e4m3 scale byte and 8 code bytes.
+__device__ __forceinline__ void quantize_block16(const float (&f)[16], float gs, uint2& codes,
+                                                 uint8_t& scale) {
+  float amax_b = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax_b = fmaxf(amax_b, fabsf(f[i]));
+  const uint32_t sbyte = to_e4m3(__fdiv_rn(__fmul_rn(amax_b, gs), 6.0f));
+  uint32_t packed[2] = {0u, 0u};
+  // zero scale: all codes +0; a NaN scale (only from non-finite weights,
+  // which the format does not cover) likewise
+  if (sbyte != 0u && sbyte != 0x7Fu) {
+    const ScaleDiv sd = scale_div(sbyte);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t byte = to_e2m1x2(div_by_scale(__fmul_rn(f[2 * i], gs), sd),
+                                      div_by_scale(__fmul_rn(f[2 * i + 1], gs), sd));
+      packed[i >> 2] |= byte << (8 * (i & 3));
+    }
+  }
+  codes = make_uint2(packed[0], packed[1]);
+  scale = static_cast<uint8_t>(sbyte);
+}
+
 // One thread per 16-input block: n_blocks = N * K / 16 in row-major order.
 __global__ void __launch_bounds__(kThreads)
     quantize_kernel(const uint4* __restrict__ w, int64_t n_blocks,
@@ -118,28 +144,104 @@ __global__ void __launch_bounds__(kThreads)
     const uint4 v0 = w[2 * b], v1 = w[2 * b + 1];
     const uint32_t words[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
     float f[16];
-    float amax_b = 0.0f;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       f[2 * i] = __uint_as_float(words[i] << 16);
       f[2 * i + 1] = __uint_as_float(words[i] & 0xFFFF0000u);
-      amax_b = fmaxf(amax_b, fmaxf(fabsf(f[2 * i]), fabsf(f[2 * i + 1])));
     }
-    const uint32_t sbyte = to_e4m3(__fdiv_rn(__fmul_rn(amax_b, gs), 6.0f));
-    uint32_t packed[2] = {0u, 0u};
-    // zero scale: all codes +0; a NaN scale (only from non-finite weights,
-    // which the format does not cover) likewise
-    if (sbyte != 0u && sbyte != 0x7Fu) {
-      const ScaleDiv sd = scale_div(sbyte);
+    uint2 c;
+    uint8_t sc;
+    quantize_block16(f, gs, c, sc);
+    codes[b] = c;
+    scales[b] = sc;
+  }
+}
+
+// ---------------------------------------------------------------- FP8 source
+// A block-scaled FP8 checkpoint tensor (e4m3 codes, one fp32 scale_inv per
+// B x B block) goes FP8 -> BF16 -> NVFP4 (FlashRT docs, the MTP-head note:
+// FP8 e4m3 in blocks of 128, converted once at load; qwentin README,
+// "Convert a model": block-scaled E4M3 tensors are dequantised first).  The
+// bf16 image of each weight, RNE_bf16(e4m3 * scale_inv), is formed on the
+// fly in both passes, so no bf16 copy of the tensor is stored.
+struct Fp8Layout {
+  int64_t n_blocks;     // N * K / 16
+  int64_t k_blocks;     // K / 16 (16-input blocks per row)
+  int64_t kb;           // ceil(K / B): scale_inv row length
+  int64_t B;            // scale block edge (a multiple of 16)
+};
+
+// Two e4m3 bytes (the low byte -> .x) as fp32, exactly.
+__device__ __forceinline__ float2 e4m3x2_to_f32(uint32_t two) {
+  uint32_t h;
+  asm("{\n\t.reg .b16 s;\n\t"
+      "cvt.u16.u32 s, %1;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, s;\n\t}"
+      : "=r"(h)
+      : "r"(two));
+  return __half22float2(*reinterpret_cast<const __half2*>(&h));
+}
+
+// The bf16 images (as fp32) of the 16 FP8 weights of 16-input block b.
+__device__ __forceinline__ void fp8_block16(const uint4* __restrict__ w8,
+                                            const float* __restrict__ scale_inv,
+                                            const Fp8Layout& L, int64_t b, float (&f)[16]) {
+  const int64_t row = b / L.k_blocks;
+  const int64_t k0 = (b - row * L.k_blocks) * 16;
+  const float s = scale_inv[(row / L.B) * L.kb + k0 / L.B];
+  const uint4 v = w8[b];
+  const uint32_t words[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const uint32_t byte = to_e2m1x2(div_by_scale(__fmul_rn(f[2 * i], gs), sd),
-                                        div_by_scale(__fmul_rn(f[2 * i + 1], gs), sd));
-        packed[i >> 2] |= byte << (8 * (i & 3));
-      }
-    }
-    codes[b] = make_uint2(packed[0], packed[1]);
-    scales[b] = static_cast<uint8_t>(sbyte);
+  for (int i = 0; i < 4; ++i) {
+    const float2 lo = e4m3x2_to_f32(words[i] & 0xFFFFu);
+    const float2 hi = e4m3x2_to_f32(words[i] >> 16);
+    f[4 * i] = __bfloat162float(__float2bfloat16_rn(__fmul_rn(lo.x, s)));
+    f[4 * i + 1] = __bfloat162float(__float2bfloat16_rn(__fmul_rn(lo.y, s)));
+    f[4 * i + 2] = __bfloat162float(__float2bfloat16_rn(__fmul_rn(hi.x, s)));
+    f[4 * i + 3] = __bfloat162float(__float2bfloat16_rn(__fmul_rn(hi.y, s)));
+  }
+}
+
+// |w| maximum of the bf16 images, into *amax_bits (zeroed before).
+__global__ void __launch_bounds__(kThreads) amax_fp8_kernel(const uint4* __restrict__ w8,
+                                                            const float* __restrict__ scale_inv,
+                                                            Fp8Layout L,
+                                                            unsigned int* amax_bits) {
+  float m = 0.0f;
+  for (int64_t b = blockIdx.x * static_cast<int64_t>(kThreads) + threadIdx.x; b < L.n_blocks;
+       b += static_cast<int64_t>(gridDim.x) * kThreads) {
+    float f[16];
+    fp8_block16(w8, scale_inv, L, b, f);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(f[i]));
+  }
+  // non-negative floats order like their bit patterns
+  uint32_t u = __reduce_max_sync(0xffffffffu, __float_as_uint(m));
+  __shared__ uint32_t red[kThreads / 32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) red[warp] = u;
+  __syncthreads();
+  if (warp == 0) {
+    u = lane < kThreads / 32 ? red[lane] : 0u;
+    u = __reduce_max_sync(0xffffffffu, u);
+    if (lane == 0 && u != 0) atomicMax(amax_bits, u);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads)
+    quantize_fp8_kernel(const uint4* __restrict__ w8, const float* __restrict__ scale_inv,
+                        Fp8Layout L, const unsigned int* __restrict__ amax_bits,
+                        uint2* __restrict__ codes, uint8_t* __restrict__ scales) {
+  const float gs = global_scale_of(__uint_as_float(*amax_bits));
+  for (int64_t b = blockIdx.x * static_cast<int64_t>(kThreads) + threadIdx.x; b < L.n_blocks;
+       b += static_cast<int64_t>(gridDim.x) * kThreads) {
+    float f[16];
+    fp8_block16(w8, scale_inv, L, b, f);
+    uint2 c;
+    uint8_t sc;
+    quantize_block16(f, gs, c, sc);
+    codes[b] = c;
+    scales[b] = sc;
   }
 }
 

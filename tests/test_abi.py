@@ -139,6 +139,14 @@ def test_rejects_before_any_device_work(lib):
     assert q(A, 4, 40, A, A, F, None) == -3                  # K % 16
     assert q(A + 8, 4, 64, A, A, F, None) == -2               # w not 16-byte aligned
     assert q(A, 4, 64, A + 4, A, F, None) == -2               # codes not 8-byte aligned
+    q8 = lib.nvfp4_quantize_fp8
+    assert q8(None, F, 128, 4, 64, A, A, F, None) == -1
+    assert q8(A, None, 128, 4, 64, A, A, F, None) == -1
+    assert q8(A, F, 0, 4, 64, A, A, F, None) == -1
+    assert q8(A, F, 128, 4, 40, A, A, F, None) == -3           # K % 16
+    assert q8(A, F, 100, 4, 64, A, A, F, None) == -3           # block % 16
+    assert q8(A + 8, F, 128, 4, 64, A, A, F, None) == -2       # codes not 16-byte aligned
+    assert q8(A, F + 2, 128, 4, 64, A, A, F, None) == -2       # scale_inv misaligned
     h = lib.nvfp4_linear_host
     H = 0x30000            # fake host address, never dereferenced
     assert h(None, A, A, A, ctypes.c_float(1.0), A, H, 1, 256, 512, 0, None) == -1

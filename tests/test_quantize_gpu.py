@@ -85,3 +85,44 @@ def test_quantised_weights_drive_the_linear():
     wp_o, ws_o, gs_o = oracle.quantize(bits)
     y64, a = oracle.linear_f64(x_bits, wp_o, ws_o, gs_o)
     check_f32(y.cpu().numpy(), y64, a, "quantise then linear")
+
+
+# ------------------------------------------------------------------ FP8 source
+def _fp8_case(N, K, block, seed):
+    """Block-scaled FP8 weights shaped like a checkpoint tensor: e4m3 codes of
+    N(0, 1) values (NaN codes excluded) and one fp32 scale_inv per block."""
+    rng = np.random.default_rng(seed)
+    w = torch.from_numpy(rng.standard_normal((N, K)).astype(np.float32) * 60.0)
+    w8 = w.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    nb, kb = -(-N // block), -(-K // block)
+    sinv = np.exp(rng.uniform(-9, 2, size=(nb, kb))).astype(np.float32)
+    return np.ascontiguousarray(w8), sinv
+
+
+@pytest.mark.parametrize("N,K,block", [(1, 16, 16), (7, 48, 16), (200, 272, 128),
+                                       (300, 1024, 128), (129, 4096, 64), (2048, 5120, 128)])
+def test_quantize_fp8_bit_exact(N, K, block):
+    w8, sinv = _fp8_case(N, K, block, seed=N + K + block)
+    wp, ws, gs = _lib.quantize_fp8(torch.from_numpy(w8).to(DEV), torch.from_numpy(sinv).to(DEV),
+                                   block)
+    torch.cuda.synchronize()
+    wp_o, ws_o, gs_o = oracle.quantize_fp8(w8, sinv, block)
+    assert np.float32(gs.cpu().numpy()[0]) == gs_o
+    assert np.array_equal(ws.cpu().numpy(), ws_o)
+    assert np.array_equal(wp.cpu().numpy(), wp_o)
+
+
+def test_quantize_fp8_equals_bf16_quantiser_on_the_converted_tensor():
+    """The FP8 entry point equals nvfp4_quantize applied to the bf16 tensor
+    torch converts from the same FP8 codes and scales (both on the GPU)."""
+    N, K, block = 384, 2048, 128
+    w8, sinv = _fp8_case(N, K, block, seed=31)
+    w8_t = torch.from_numpy(w8).to(DEV)
+    s_t = torch.from_numpy(sinv).to(DEV)
+    s_full = s_t.repeat_interleave(block, 0)[:N].repeat_interleave(block, 1)[:, :K]
+    w_bf16 = (w8_t.view(torch.float8_e4m3fn).to(torch.float32) * s_full).to(torch.bfloat16)
+    a = _lib.quantize_fp8(w8_t.view(torch.float8_e4m3fn), s_t, block)
+    b = _lib.quantize(w_bf16.contiguous())
+    torch.cuda.synchronize()
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
