@@ -981,6 +981,9 @@ int nvfp4_quantize_fp8(const uint8_t* w_fp8, const float* scale_inv, int64_t blo
   L.k_blocks = K / 16;
   L.kb = (K + block - 1) / block;
   L.B = block;
+  L.b_shift = -1;
+  for (int sh = 4; sh < 31; ++sh)
+    if ((int64_t(1) << sh) == block) L.b_shift = sh;
   const int64_t grid_cap = static_cast<int64_t>(d->num_sms) * 8;
   const unsigned grid = static_cast<unsigned>(
       std::min<int64_t>(grid_cap, (L.n_blocks + Q::kThreads - 1) / Q::kThreads));

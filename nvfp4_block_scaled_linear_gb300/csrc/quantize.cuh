@@ -169,6 +169,31 @@ struct Fp8Layout {
   int64_t k_blocks;     // K / 16 (16-input blocks per row)
   int64_t kb;           // ceil(K / B): scale_inv row length
   int64_t B;            // scale block edge (a multiple of 16)
+  int b_shift;          // log2(B) when B is a power of two, else -1
+};
+
+// Position of 16-input block b (row, k-block) and of its scale, walked
+// forward by a fixed stride: one division per thread, not per block.
+struct Fp8Cursor {
+  int64_t b, row, kblk;
+  int64_t d_row, d_kblk;    // the stride as (rows, k-blocks)
+  __device__ Fp8Cursor(const Fp8Layout& L, int64_t start, int64_t stride)
+      : b(start), row(start / L.k_blocks), kblk(start - (start / L.k_blocks) * L.k_blocks),
+        d_row(stride / L.k_blocks), d_kblk(stride - (stride / L.k_blocks) * L.k_blocks) {}
+  __device__ __forceinline__ void advance(const Fp8Layout& L, int64_t stride) {
+    b += stride;
+    row += d_row;
+    kblk += d_kblk;
+    if (kblk >= L.k_blocks) {
+      kblk -= L.k_blocks;
+      ++row;
+    }
+  }
+  __device__ __forceinline__ int64_t scale_index(const Fp8Layout& L) const {
+    if (L.b_shift >= 0)
+      return (row >> L.b_shift) * L.kb + ((kblk * 16) >> L.b_shift);
+    return (row / L.B) * L.kb + (kblk * 16) / L.B;
+  }
 };
 
 // Two e4m3 bytes (the low byte -> .x) as fp32, exactly.
@@ -182,14 +207,13 @@ __device__ __forceinline__ float2 e4m3x2_to_f32(uint32_t two) {
   return __half22float2(*reinterpret_cast<const __half2*>(&h));
 }
 
-// The bf16 images (as fp32) of the 16 FP8 weights of 16-input block b.
+// The bf16 images (as fp32) of the 16 FP8 weights of the cursor's block.
 __device__ __forceinline__ void fp8_block16(const uint4* __restrict__ w8,
                                             const float* __restrict__ scale_inv,
-                                            const Fp8Layout& L, int64_t b, float (&f)[16]) {
-  const int64_t row = b / L.k_blocks;
-  const int64_t k0 = (b - row * L.k_blocks) * 16;
-  const float s = scale_inv[(row / L.B) * L.kb + k0 / L.B];
-  const uint4 v = w8[b];
+                                            const Fp8Layout& L, const Fp8Cursor& c,
+                                            float (&f)[16]) {
+  const float s = scale_inv[c.scale_index(L)];
+  const uint4 v = w8[c.b];
   const uint32_t words[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
@@ -202,18 +226,26 @@ __device__ __forceinline__ void fp8_block16(const uint4* __restrict__ w8,
   }
 }
 
-// |w| maximum of the bf16 images, into *amax_bits (zeroed before).
+// |w| maximum of the bf16 images, into *amax_bits (zeroed before).  Both
+// roundings are monotone, so a block's largest |bf16 image| is the image of
+// its largest e4m3 magnitude: RN_bf16(RN_fp32(max|e4m3| * |scale_inv|)).
+// e4m3 magnitudes order like their 7-bit patterns, so the block maximum is
+// a byte-wise integer maximum and one conversion per 16 weights.
 __global__ void __launch_bounds__(kThreads) amax_fp8_kernel(const uint4* __restrict__ w8,
                                                             const float* __restrict__ scale_inv,
                                                             Fp8Layout L,
                                                             unsigned int* amax_bits) {
   float m = 0.0f;
-  for (int64_t b = blockIdx.x * static_cast<int64_t>(kThreads) + threadIdx.x; b < L.n_blocks;
-       b += static_cast<int64_t>(gridDim.x) * kThreads) {
-    float f[16];
-    fp8_block16(w8, scale_inv, L, b, f);
-#pragma unroll
-    for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(f[i]));
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+  for (Fp8Cursor c(L, blockIdx.x * static_cast<int64_t>(kThreads) + threadIdx.x, stride);
+       c.b < L.n_blocks; c.advance(L, stride)) {
+    const uint4 v = w8[c.b];
+    uint32_t mx = __vmaxu4(__vmaxu4(v.x & 0x7F7F7F7Fu, v.y & 0x7F7F7F7Fu),
+                           __vmaxu4(v.z & 0x7F7F7F7Fu, v.w & 0x7F7F7F7Fu));
+    mx = max(max(mx & 0xFFu, (mx >> 8) & 0xFFu), max((mx >> 16) & 0xFFu, mx >> 24));
+    const float a = e4m3x2_to_f32(mx).x;
+    const float sabs = fabsf(scale_inv[c.scale_index(L)]);
+    m = fmaxf(m, __bfloat162float(__float2bfloat16_rn(__fmul_rn(a, sabs))));
   }
   // non-negative floats order like their bit patterns
   uint32_t u = __reduce_max_sync(0xffffffffu, __float_as_uint(m));
@@ -233,15 +265,16 @@ __global__ void __launch_bounds__(kThreads)
                         Fp8Layout L, const unsigned int* __restrict__ amax_bits,
                         uint2* __restrict__ codes, uint8_t* __restrict__ scales) {
   const float gs = global_scale_of(__uint_as_float(*amax_bits));
-  for (int64_t b = blockIdx.x * static_cast<int64_t>(kThreads) + threadIdx.x; b < L.n_blocks;
-       b += static_cast<int64_t>(gridDim.x) * kThreads) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kThreads;
+  for (Fp8Cursor c(L, blockIdx.x * static_cast<int64_t>(kThreads) + threadIdx.x, stride);
+       c.b < L.n_blocks; c.advance(L, stride)) {
     float f[16];
-    fp8_block16(w8, scale_inv, L, b, f);
-    uint2 c;
+    fp8_block16(w8, scale_inv, L, c, f);
+    uint2 cw;
     uint8_t sc;
-    quantize_block16(f, gs, c, sc);
-    codes[b] = c;
-    scales[b] = sc;
+    quantize_block16(f, gs, cw, sc);
+    codes[c.b] = cw;
+    scales[c.b] = sc;
   }
 }
 
