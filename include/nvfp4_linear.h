@@ -203,9 +203,10 @@ int nvfp4_quantize_fp8(const uint8_t* w_fp8, const float* scale_inv, int64_t blo
                        int64_t K, uint8_t* w_packed, uint8_t* w_scale, float* global_scale,
                        void* stream);
 
-/* General form of the four calls above; `flags` is an OR of NVFP4_FLAG_*.
+/* General form of nvfp4_linear, _f32, _swiglu and _swiglu_f32; `flags` is
+ * an OR of NVFP4_FLAG_*.
  * The FORCE flags pick a kernel regardless of M (for A/B measurements and
- * for checking both kernels on the same inputs). */
+ * for checking the kernels against each other on the same inputs). */
 int nvfp4_linear_ex(const void* x, const uint8_t* w_packed, const uint8_t* w_scale,
                     float global_scale, void* y, int64_t M, int64_t N, int64_t K,
                     unsigned int flags, void* stream);
