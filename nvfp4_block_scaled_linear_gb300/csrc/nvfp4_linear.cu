@@ -38,26 +38,27 @@ constexpr int64_t kSmallMMax = 32;
 
 using SmallmFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, sm::Params);
 
-// The few-row kernel instance for (MT, G, f16); combinations the kernel does
-// not support are never instantiated.
-template <int MT, int G, bool F16>
+// The few-row kernel instance for (MT, G, CV) (CV: 0 bf16, 1 or 2 f16 with
+// that many activation converters); combinations the kernel does not
+// support are never instantiated.
+template <int MT, int G, int CV>
 constexpr SmallmFn smallm_instance() {
-  if constexpr (G <= sm::max_groups(MT) && (!F16 || MT == 1))
-    return &sm::smallm_kernel<MT, G, F16>;
+  if constexpr (G <= sm::max_groups(MT) && (CV == 0 || MT == 1))
+    return &sm::smallm_kernel<MT, G, CV>;
   else
     return nullptr;
 }
-template <int MT, bool F16>
+template <int MT, int CV>
 SmallmFn smallm_fn(int g) {
   switch (g) {
-    case 1: return smallm_instance<MT, 1, F16>();
-    case 2: return smallm_instance<MT, 2, F16>();
-    case 3: return smallm_instance<MT, 3, F16>();
-    case 4: return smallm_instance<MT, 4, F16>();
-    case 5: return smallm_instance<MT, 5, F16>();
-    case 6: return smallm_instance<MT, 6, F16>();
-    case 7: return smallm_instance<MT, 7, F16>();
-    case 8: return smallm_instance<MT, 8, F16>();
+    case 1: return smallm_instance<MT, 1, CV>();
+    case 2: return smallm_instance<MT, 2, CV>();
+    case 3: return smallm_instance<MT, 3, CV>();
+    case 4: return smallm_instance<MT, 4, CV>();
+    case 5: return smallm_instance<MT, 5, CV>();
+    case 6: return smallm_instance<MT, 6, CV>();
+    case 7: return smallm_instance<MT, 7, CV>();
+    case 8: return smallm_instance<MT, 8, CV>();
     default: return nullptr;
   }
 }
@@ -69,7 +70,7 @@ struct DeviceInfo {
   int max_smem = 0;                    // opt-in shared memory per block
   int smem_per_sm = 0, smem_reserved = 0, regs_per_sm = 0, threads_per_sm = 0;
   unsigned int* err = nullptr;         // device address of g_device_error
-  int smallm_regs[2][5][sm::kMaxGroups + 1] = {};  // registers per thread by (f16, MT, G)
+  int smallm_regs[3][5][sm::kMaxGroups + 1] = {};  // registers per thread by (CV, MT, G)
   int gemv_regs[2] = {};               // registers per thread of the tcgen05 few-row kernel (N 16, 32)
   int gemv_bf16_regs[2][2] = {};       // the same, bf16 kernel, by (N 16 / 32, lane groups 2 / 4)
 };
@@ -78,10 +79,10 @@ std::mutex g_mutex;
 DeviceInfo g_dev[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
-template <int MT, bool F16>
+template <int MT, int CV>
 cudaError_t prepare_smallm(DeviceInfo& d) {
   for (int g = 1; g <= sm::max_groups(MT); ++g) {
-    const SmallmFn kern = smallm_fn<MT, F16>(g);
+    const SmallmFn kern = smallm_fn<MT, CV>(g);
     if (!kern) continue;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, d.max_smem);
@@ -90,7 +91,7 @@ cudaError_t prepare_smallm(DeviceInfo& d) {
     cudaFuncAttributes fa;
     if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, kern);
     if (e != cudaSuccess) return e;
-    d.smallm_regs[F16 ? 1 : 0][MT][g] = fa.numRegs;
+    d.smallm_regs[CV][MT][g] = fa.numRegs;
   }
   return cudaSuccess;
 }
@@ -170,11 +171,12 @@ int device_setup(DeviceInfo** out) {
       }
       void* err_addr = nullptr;
       if (cudaGetSymbolAddress(&err_addr, g_device_error) != cudaSuccess ||
-          prepare_smallm<1, false>(d) != cudaSuccess ||
-          prepare_smallm<2, false>(d) != cudaSuccess ||
-          prepare_smallm<3, false>(d) != cudaSuccess ||
-          prepare_smallm<4, false>(d) != cudaSuccess ||
-          prepare_smallm<1, true>(d) != cudaSuccess ||
+          prepare_smallm<1, 0>(d) != cudaSuccess ||
+          prepare_smallm<2, 0>(d) != cudaSuccess ||
+          prepare_smallm<3, 0>(d) != cudaSuccess ||
+          prepare_smallm<4, 0>(d) != cudaSuccess ||
+          prepare_smallm<1, 1>(d) != cudaSuccess ||
+          prepare_smallm<1, 2>(d) != cudaSuccess ||
           prepare_gemv<16>(d) != cudaSuccess || prepare_gemv<32>(d) != cudaSuccess ||
           prepare_gemv_bf16<16, 2>(d) != cudaSuccess ||
           prepare_gemv_bf16<16, 4>(d) != cudaSuccess ||
@@ -390,7 +392,7 @@ struct SmallmPlan {
 // the rings of an SM hold less than ~128 KB of weights in flight; grids that
 // are resident in one wave win over those that are not; ties go to fewer
 // CTAs.  Overrides in `flags` pin G or the split.
-template <int MT, bool F16>
+template <int MT, int CV>
 SmallmPlan plan_smallm(const DeviceInfo& d, int64_t M, int64_t N, int64_t K,
                        unsigned int flags) {
   const bool swiglu = flags & NVFP4_FLAG_SWIGLU;
@@ -398,7 +400,8 @@ SmallmPlan plan_smallm(const DeviceInfo& d, int64_t M, int64_t N, int64_t K,
   const int want_split = (flags & NVFP4_FLAG_SPLIT_MASK) >> NVFP4_FLAG_SPLIT_SHIFT;
   const int want_groups = (flags & NVFP4_FLAG_GROUPS_MASK) >> NVFP4_FLAG_GROUPS_SHIFT;
   const int64_t unit_rows = swiglu ? N / 2 : N;
-  const int threads = sm::threads_for(F16);
+  constexpr bool F16 = CV > 0;
+  const int threads = sm::threads_for(CV);
   static const int kStageChoices[] = {3, 4, 5, 6, 8};
   SmallmPlan best;
   double best_cost = -1.0;
@@ -406,7 +409,7 @@ SmallmPlan plan_smallm(const DeviceInfo& d, int64_t M, int64_t N, int64_t K,
   bool best_one_wave = false;
   for (int g = 1; g <= sm::max_groups(MT); ++g) {
     if (want_groups && g != want_groups) continue;
-    const int regs = d.smallm_regs[F16 ? 1 : 0][MT][g];
+    const int regs = d.smallm_regs[CV][MT][g];
     if (regs <= 0) continue;
     const int64_t rows_per_cta = swiglu ? 8 * g : 16 * g;
     const int64_t row_blocks = (unit_rows + rows_per_cta - 1) / rows_per_cta;
@@ -448,14 +451,15 @@ SmallmPlan plan_smallm(const DeviceInfo& d, int64_t M, int64_t N, int64_t K,
   return best;
 }
 
-template <int MT, bool F16>
+template <int MT, int CV>
 int launch_smallm(const DeviceInfo& d, const void* x, const uint8_t* wp, const uint8_t* ws,
                   float gs, float gs_up, void* y, int64_t M, int64_t N, int64_t K, unsigned int flags,
                   cudaStream_t stream, const SegSpec* segs) {
+  constexpr bool F16 = CV > 0;
   const bool swiglu = flags & NVFP4_FLAG_SWIGLU;
   static PlanMemo<SmallmPlan> memo;
   const SmallmPlan plan =
-      memo.get(d, M, N, K, flags, [&] { return plan_smallm<MT, F16>(d, M, N, K, flags); });
+      memo.get(d, M, N, K, flags, [&] { return plan_smallm<MT, CV>(d, M, N, K, flags); });
   if (plan.groups == 0) return NVFP4_ERR_INVALID;   // overrides that cannot run
   const int half_rows = 8 * plan.groups;
   CUtensorMap tw, ts, tx;
@@ -490,7 +494,7 @@ int launch_smallm(const DeviceInfo& d, const void* x, const uint8_t* wp, const u
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof cfg);
   cfg.gridDim = dim3(static_cast<unsigned>(plan.row_blocks), static_cast<unsigned>(plan.split), 1);
-  cfg.blockDim = dim3(sm::threads_for(F16), 1, 1);
+  cfg.blockDim = dim3(sm::threads_for(CV), 1, 1);
   cfg.dynamicSmemBytes = p.lay.total;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
@@ -505,7 +509,7 @@ int launch_smallm(const DeviceInfo& d, const void* x, const uint8_t* wp, const u
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   const cudaError_t e =
-      cudaLaunchKernelEx(&cfg, smallm_fn<MT, F16>(plan.groups), tw, ts, tx, p);
+      cudaLaunchKernelEx(&cfg, smallm_fn<MT, CV>(plan.groups), tw, ts, tx, p);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return NVFP4_ERR_LAUNCH;
@@ -812,12 +816,17 @@ int run(const void* x, const uint8_t* wp, const uint8_t* ws, float gs, float gs_
   if (kernel == NVFP4_KERNEL_SMALLM) {
     switch ((M + 7) / 8) {
       case 1:
-        if (!(flags & NVFP4_FLAG_BF16_MMA))
-          return launch_smallm<1, true>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs);
-        return launch_smallm<1, false>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs);
-      case 2: return launch_smallm<2, false>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs);
-      case 3: return launch_smallm<3, false>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs);
-      default: return launch_smallm<4, false>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs);
+        // f16 with one activation converter up to M = 3, two from M = 4
+        // (verify, M = 7: 19.5 us against 22.4 with one; M = 5: 18.4
+        // against 19.6; decode, M = 1: 21.8 against 22.4 with two)
+        if (flags & NVFP4_FLAG_BF16_MMA)
+          return launch_smallm<1, 0>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs);
+        if (M <= 3)
+          return launch_smallm<1, 1>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs);
+        return launch_smallm<1, 2>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs);
+      case 2: return launch_smallm<2, 0>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs);
+      case 3: return launch_smallm<3, 0>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs);
+      default: return launch_smallm<4, 0>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs);
     }
   }
   return launch_tcgemm(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs);

@@ -54,10 +54,8 @@ constexpr int kConsumerWarps = 8;     // (k quarter, row-group parity)
 constexpr int kMaxSplit = 16;         // cluster size limit (non-portable above 8)
 constexpr int kF16MaxRows = 8;        // the f16 path serves M <= 8
 
-// Consumers, the TMA producer and (f16 path) the activation converter.
-__host__ __device__ constexpr int threads_for(bool f16) {
-  return (kConsumerWarps + 1 + (f16 ? 1 : 0)) * 32;
-}
+// Consumers, the TMA producer and (f16 path) cv activation converters.
+__host__ __device__ constexpr int threads_for(int cv) { return (kConsumerWarps + 1 + cv) * 32; }
 
 // Row groups one consumer warp may hold: all of its accumulators live in
 // registers, so the widest activation tiles get fewer.
@@ -149,12 +147,15 @@ __device__ __forceinline__ int next_slot(int slot, int stages, uint32_t& parity)
   return slot;
 }
 
-template <int MT, int G, bool F16>
-__global__ void __launch_bounds__(threads_for(F16), F16 ? 2 : 1)
+// CV: 0 for the bf16 path; 1 or 2 for the f16 path with that many
+// activation converter warps (two pay from M = 4 on, one is faster below).
+template <int MT, int G, int CV>
+__global__ void __launch_bounds__(threads_for(CV), CV > 0 ? 2 : 1)
     smallm_kernel(const __grid_constant__ CUtensorMap tm_w,
                   const __grid_constant__ CUtensorMap tm_s,
                   const __grid_constant__ CUtensorMap tm_x, const Params p) {
-  constexpr int kThreads = threads_for(F16);
+  constexpr bool F16 = CV > 0;
+  constexpr int kThreads = threads_for(CV);
   constexpr int RG = groups_per_warp(MT);
   constexpr int C = MT * 8;
   constexpr int rows = G * kGroupRows;
@@ -195,8 +196,8 @@ __global__ void __launch_bounds__(threads_for(F16), F16 ? 2 : 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < L.stages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&conv[s], 1);
-      mbar_init(&empty[s], kConsumerWarps + (F16 ? 1 : 0));
+      mbar_init(&conv[s], CV > 0 ? CV : 1);
+      mbar_init(&empty[s], kConsumerWarps + CV);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -268,43 +269,86 @@ __global__ void __launch_bounds__(threads_for(F16), F16 ? 2 : 1)
           atomicOr(p.err, kErrWaitTimeout);
       }
     }
-  } else if (F16 && warp == kConsumerWarps + 1) {
-    // ------------------------------------------------------------ converter
-    // Lane l takes the 16-byte chunk l (8 consecutive k) of every activation
-    // row of every stage.  a_run[m] is row m's exponent: x is stored as
-    // f16(x * 2^a_run), with a_run the largest value keeping the row's
-    // running maximum below 2^15 (so no f16 overflow).
+  } else if (F16 && warp > kConsumerWarps) {
+    // ------------------------------------------------------------ converters
+    // Converter c takes activation rows c, c + CV, ...: one converter up to
+    // M = 3, row after row; two from M = 4, each converting all of its rows
+    // at once so that their load -> max -> convert chains overlap (one warp
+    // for all the rows bounded the verify launch).  Lane l takes the 16-byte
+    // chunk l (8 consecutive k) of each row of every stage.  a_run[i] is the
+    // exponent of row c + CV * i: x is stored as f16(x * 2^a_run), with
+    // a_run the largest value keeping the row's running maximum below 2^15
+    // (so no f16 overflow).
+    constexpr int kConvWarps = CV > 0 ? CV : 1;
+    constexpr int kRowsPer = kF16MaxRows / kConvWarps;
+    const int c = warp - kConsumerWarps - 1;
     const int M = static_cast<int>(p.M);
-    int a_run[kF16MaxRows];
+    // this converter's rows (warp-uniform); the warp-wide maximum is not
+    // cheap, and the conversion is on every stage's critical path: rows
+    // past M are skipped, not processed as zeros
+    const int n_rows = M > c ? (M - c + kConvWarps - 1) / kConvWarps : 0;
+    // row m of the stage (this lane's 8 k) -> f16(x * 2^a) in the swizzled
+    // operand tile; lane 0 records the row's exponent.  (max * 2^a < 2^15.)
+    auto convert_row = [&](uint8_t* st, int m, const uint4& v, int a) {
+      const float f = pow2f(a);
+      const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+      uint32_t o[4];
 #pragma unroll
-    for (int m = 0; m < kF16MaxRows; ++m) a_run[m] = 126;
+      for (int j = 0; j < 4; ++j)
+        o[j] = f32x2_to_f16x2(__uint_as_float(w4[j] << 16) * f,
+                              __uint_as_float(w4[j] & 0xFFFF0000u) * f);
+      *reinterpret_cast<uint4*>(st + L.x16_off + m * 512 + ((lane ^ (m & 7)) << 4)) =
+          make_uint4(o[0], o[1], o[2], o[3]);
+      if (lane == 0) reinterpret_cast<int*>(st + L.exp_off)[m] = a;
+    };
+    int a_run[kRowsPer];
+#pragma unroll
+    for (int i = 0; i < kRowsPer; ++i) a_run[i] = 126;
     int slot = 0;                 // ring position, stepped without a divide
     uint32_t par = 0;
     for (int it = 0; it < n_stages; ++it, slot = next_slot(slot, L.stages, par)) {
       if (!mbar_wait(&full[slot], par, abort_flag)) break;
       uint8_t* st = smem + slot * L.stage_bytes;
+      if constexpr (CV == 1) {
+        // one converter (M <= 3): row after row
 #pragma unroll
-      for (int m = 0; m < kF16MaxRows; ++m) {
-        if (m >= M) break;
-        const uint4 v = *reinterpret_cast<const uint4*>(st + L.x_off + m * 512 + lane * 16);
-        uint32_t mx = max_u16x2(max_u16x2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
-                                max_u16x2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
-        mx = __reduce_max_sync(0xffffffffu, max(mx & 0xFFFFu, mx >> 16));
-        const int e_max = static_cast<int>(mx >> 7);         // biased bf16 exponent
-        a_run[m] = min(a_run[m], max(-126, 141 - e_max));    // max * 2^a < 2^15
-        const float f = pow2f(a_run[m]);
-        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-        uint32_t o[4];
+        for (int i = 0; i < kRowsPer; ++i) {
+          if (i >= n_rows) break;
+          const uint4 v = *reinterpret_cast<const uint4*>(st + L.x_off + i * 512 + lane * 16);
+          uint32_t mx = max_u16x2(max_u16x2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
+                                  max_u16x2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
+          mx = __reduce_max_sync(0xffffffffu, max(mx & 0xFFFFu, mx >> 16));
+          a_run[i] = min(a_run[i], max(-126, 141 - static_cast<int>(mx >> 7)));
+          convert_row(st, i, v, a_run[i]);
+        }
+      } else {
+        // several converters (M >= 4): each converts all of its rows at once
+        uint4 v[kRowsPer];
+        int e_max[kRowsPer];
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          o[j] = f32x2_to_f16x2(__uint_as_float(w4[j] << 16) * f,
-                                __uint_as_float(w4[j] & 0xFFFF0000u) * f);
-        *reinterpret_cast<uint4*>(st + L.x16_off + m * 512 + ((lane ^ (m & 7)) << 4)) =
-            make_uint4(o[0], o[1], o[2], o[3]);
-        if (lane == 0) reinterpret_cast<int*>(st + L.exp_off)[m] = a_run[m];
+        for (int i = 0; i < kRowsPer; ++i) {
+          if (i >= n_rows) break;
+          v[i] = *reinterpret_cast<const uint4*>(st + L.x_off + (c + kConvWarps * i) * 512 +
+                                                 lane * 16);
+        }
+#pragma unroll
+        for (int i = 0; i < kRowsPer; ++i) {
+          if (i >= n_rows) break;
+          uint32_t mx = max_u16x2(max_u16x2(v[i].x & 0x7FFF7FFFu, v[i].y & 0x7FFF7FFFu),
+                                  max_u16x2(v[i].z & 0x7FFF7FFFu, v[i].w & 0x7FFF7FFFu));
+          mx = __reduce_max_sync(0xffffffffu, max(mx & 0xFFFFu, mx >> 16));
+          e_max[i] = static_cast<int>(mx >> 7);                // biased bf16 exponent
+        }
+#pragma unroll
+        for (int i = 0; i < kRowsPer; ++i) {
+          if (i >= n_rows) break;
+          a_run[i] = min(a_run[i], max(-126, 141 - e_max[i]));
+          convert_row(st, c + kConvWarps * i, v[i], a_run[i]);
+        }
       }
       // rows past M: a fixed exponent (their columns hold zeros)
-      if (lane >= M && lane < kF16MaxRows) reinterpret_cast<int*>(st + L.exp_off)[lane] = 126;
+      if (c == 0 && lane >= M && lane < kF16MaxRows)
+        reinterpret_cast<int*>(st + L.exp_off)[lane] = 126;
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&conv[slot]);
