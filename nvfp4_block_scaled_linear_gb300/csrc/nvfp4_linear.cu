@@ -832,6 +832,22 @@ int run(const void* x, const uint8_t* wp, const uint8_t* ws, float gs, float gs_
   return launch_tcgemm(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs);
 }
 
+// Grid of a quantiser pass: as many CTAs as fit on the device at once (its
+// grid-stride loop then runs in one wave), fewer for a small tensor.
+template <typename Kernel>
+unsigned resident_grid(Kernel kernel, int num_sms, int64_t units) {
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, nvfp4::quant::kThreads, 0) !=
+          cudaSuccess ||
+      per_sm < 1) {
+    cudaGetLastError();
+    per_sm = 1;
+  }
+  const int64_t need = (units + nvfp4::quant::kThreads - 1) / nvfp4::quant::kThreads;
+  return static_cast<unsigned>(std::max<int64_t>(
+      1, std::min<int64_t>(static_cast<int64_t>(num_sms) * per_sm, need)));
+}
+
 }  // namespace
 
 extern "C" {
@@ -948,11 +964,8 @@ int nvfp4_quantize(const void* w, int64_t N, int64_t K, uint8_t* w_packed, uint8
   if (st != NVFP4_OK) return st;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   const int64_t n_blocks = N * (K / 16);
-  const int64_t grid_cap = static_cast<int64_t>(d->num_sms) * 8;
-  const unsigned g_amax = static_cast<unsigned>(
-      std::min<int64_t>(grid_cap, (2 * n_blocks + Q::kThreads - 1) / Q::kThreads));
-  const unsigned g_quant = static_cast<unsigned>(
-      std::min<int64_t>(grid_cap, (n_blocks + Q::kThreads - 1) / Q::kThreads));
+  const unsigned g_amax = resident_grid(Q::amax_kernel, d->num_sms, 2 * n_blocks);
+  const unsigned g_quant = resident_grid(Q::quantize_kernel, d->num_sms, n_blocks);
   unsigned int* amax_bits = reinterpret_cast<unsigned int*>(global_scale);
   if (cudaMemsetAsync(global_scale, 0, sizeof(float), stream) != cudaSuccess) {
     cudaGetLastError();
@@ -985,26 +998,45 @@ int nvfp4_quantize_fp8(const uint8_t* w_fp8, const float* scale_inv, int64_t blo
   const int st = device_setup(&d);
   if (st != NVFP4_OK) return st;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
-  Q::Fp8Layout L;
-  L.n_blocks = N * (K / 16);
-  L.k_blocks = K / 16;
-  L.kb = (K + block - 1) / block;
-  L.B = block;
-  L.b_shift = -1;
-  for (int sh = 4; sh < 31; ++sh)
-    if ((int64_t(1) << sh) == block) L.b_shift = sh;
-  const int64_t grid_cap = static_cast<int64_t>(d->num_sms) * 8;
-  const unsigned grid = static_cast<unsigned>(
-      std::min<int64_t>(grid_cap, (L.n_blocks + Q::kThreads - 1) / Q::kThreads));
+  // units of four 16-input blocks when they never cross a row or a scale
+  // block (and, for the quantiser's word-wide scale store, w_scale is 4-byte
+  // aligned); single blocks otherwise
+  const bool quad_amax = K % 64 == 0 && block % 64 == 0;
+  const bool quad_quant = quad_amax && (reinterpret_cast<uintptr_t>(w_scale) & 3u) == 0;
+  auto layout = [&](int U) {
+    Q::Fp8Layout L;
+    L.units_per_row = K / (16 * U);
+    L.n_units = N * L.units_per_row;
+    L.kb = (K + block - 1) / block;
+    L.B = block;
+    L.b_shift = -1;
+    for (int sh = 4; sh < 31; ++sh)
+      if ((int64_t(1) << sh) == block) L.b_shift = sh;
+    return L;
+  };
   unsigned int* amax_bits = reinterpret_cast<unsigned int*>(global_scale);
   if (cudaMemsetAsync(global_scale, 0, sizeof(float), stream) != cudaSuccess) {
     cudaGetLastError();
     return NVFP4_ERR_LAUNCH;
   }
   const uint4* w = reinterpret_cast<const uint4*>(w_fp8);
-  Q::amax_fp8_kernel<<<grid, Q::kThreads, 0, stream>>>(w, scale_inv, L, amax_bits);
-  Q::quantize_fp8_kernel<<<grid, Q::kThreads, 0, stream>>>(
-      w, scale_inv, L, amax_bits, reinterpret_cast<uint2*>(w_packed), w_scale);
+  uint2* codes = reinterpret_cast<uint2*>(w_packed);
+  const Q::Fp8Layout La = layout(quad_amax ? 4 : 1), Lq = layout(quad_quant ? 4 : 1);
+  const int sms = d->num_sms;
+  if (quad_amax)
+    Q::amax_fp8_kernel<4><<<resident_grid(Q::amax_fp8_kernel<4>, sms, La.n_units), Q::kThreads, 0,
+                            stream>>>(w, scale_inv, La, amax_bits);
+  else
+    Q::amax_fp8_kernel<1><<<resident_grid(Q::amax_fp8_kernel<1>, sms, La.n_units), Q::kThreads, 0,
+                            stream>>>(w, scale_inv, La, amax_bits);
+  if (quad_quant)
+    Q::quantize_fp8_kernel<4><<<resident_grid(Q::quantize_fp8_kernel<4>, sms, Lq.n_units),
+                                Q::kThreads, 0, stream>>>(w, scale_inv, Lq, amax_bits, codes,
+                                                          w_scale);
+  else
+    Q::quantize_fp8_kernel<1><<<resident_grid(Q::quantize_fp8_kernel<1>, sms, Lq.n_units),
+                                Q::kThreads, 0, stream>>>(w, scale_inv, Lq, amax_bits, codes,
+                                                          w_scale);
   Q::finalize_kernel<<<1, 32, 0, stream>>>(global_scale);
   if (cudaGetLastError() != cudaSuccess) return NVFP4_ERR_LAUNCH;
   return NVFP4_OK;

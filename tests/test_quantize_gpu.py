@@ -99,8 +99,13 @@ def _fp8_case(N, K, block, seed):
     return np.ascontiguousarray(w8), sinv
 
 
+# units of four 16-input blocks where K and block are multiples of 64
+# (300/1024/128, 129/4096/64, 2048/5120/128, 33/384/192 with a block that is
+# not a power of two), single blocks otherwise (the rest; 50/768/48: K is a
+# multiple of 64, the block is not)
 @pytest.mark.parametrize("N,K,block", [(1, 16, 16), (7, 48, 16), (200, 272, 128),
-                                       (300, 1024, 128), (129, 4096, 64), (2048, 5120, 128)])
+                                       (300, 1024, 128), (129, 4096, 64), (2048, 5120, 128),
+                                       (33, 384, 192), (50, 768, 48)])
 def test_quantize_fp8_bit_exact(N, K, block):
     w8, sinv = _fp8_case(N, K, block, seed=N + K + block)
     wp, ws, gs = _lib.quantize_fp8(torch.from_numpy(w8).to(DEV), torch.from_numpy(sinv).to(DEV),
@@ -110,6 +115,52 @@ def test_quantize_fp8_bit_exact(N, K, block):
     assert np.float32(gs.cpu().numpy()[0]) == gs_o
     assert np.array_equal(ws.cpu().numpy(), ws_o)
     assert np.array_equal(wp.cpu().numpy(), wp_o)
+
+
+@pytest.mark.parametrize("N,K,block", [(70, 512, 128), (9, 272, 16)])
+def test_quantize_fp8_edge_codes(N, K, block):
+    """FP8 bytes at the edges of the format: +-0, +-448 (the largest finite
+    e4m3), the smallest subnormals, whole zero units and blocks whose
+    largest image sets the tensor maximum; with the smallest and largest
+    tile scales."""
+    w8, sinv = _fp8_case(N, K, block, seed=N * K + 5)
+    w8[0, :64] = 0x80                                  # -0 everywhere in a unit
+    w8[1, :16] = [0x7E, 0xFE, 0x01, 0x81, 0x00, 0x80] + [0x08] * 10
+    w8[2, 16:32] = 0x01                                # subnormal-only block
+    w8[3, :] = np.where(np.arange(K) % 2 == 0, 0x7E, 0xFE)   # +-448 row
+    sinv[0, 0] = np.float32(2.0 ** -40)
+    sinv[-1, -1] = np.float32(2.0 ** 6)
+    wp, ws, gs = _lib.quantize_fp8(torch.from_numpy(w8).to(DEV), torch.from_numpy(sinv).to(DEV),
+                                   block)
+    torch.cuda.synchronize()
+    wp_o, ws_o, gs_o = oracle.quantize_fp8(w8, sinv, block)
+    assert np.float32(gs.cpu().numpy()[0]) == gs_o
+    assert np.array_equal(ws.cpu().numpy(), ws_o)
+    assert np.array_equal(wp.cpu().numpy(), wp_o)
+
+
+def test_quantize_fp8_unaligned_scale_output_takes_the_single_block_path():
+    """w_scale one byte into its allocation cannot take the four-block
+    units' word stores: the call takes single blocks and writes the same
+    bytes."""
+    import ctypes
+    N, K, block = 256, 1024, 128
+    w8, sinv = _fp8_case(N, K, block, seed=41)
+    w8_t = torch.from_numpy(w8).to(DEV)
+    s_t = torch.from_numpy(sinv).to(DEV)
+    wp_a, ws_a, gs_a = _lib.quantize_fp8(w8_t, s_t, block)
+    wp = torch.empty((N, K // 2), dtype=torch.uint8, device=DEV)
+    ws_buf = torch.full((N * (K // 16) + 16,), 0xAB, dtype=torch.uint8, device=DEV)
+    gs = torch.empty(1, dtype=torch.float32, device=DEV)
+    st = _lib.library().nvfp4_quantize_fp8(
+        w8_t.data_ptr(), s_t.data_ptr(), block, N, K, wp.data_ptr(), ws_buf.data_ptr() + 1,
+        gs.data_ptr(), ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == 0
+    torch.cuda.synchronize()
+    assert torch.equal(wp, wp_a) and torch.equal(gs, gs_a)
+    ws_u = ws_buf.cpu().numpy()
+    assert np.array_equal(ws_u[1:1 + N * (K // 16)], ws_a.cpu().numpy().ravel())
+    assert ws_u[0] == 0xAB and (ws_u[1 + N * (K // 16):] == 0xAB).all()
 
 
 def test_quantize_fp8_equals_bf16_quantiser_on_the_converted_tensor():
