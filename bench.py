@@ -336,9 +336,10 @@ def time_case(case, steps, warmup, stream, world, sampler=None, graph=True):
 def e2e_case(case, steps, stream, dev):
     """Same workload through the public API with the step's data in host
     memory: every step calls nvfp4_linear_host (through its Python binding),
-    which copies the activations in from pinned host memory, runs the layer
-    and copies the result out to pinned host memory, all inside the timed
-    region.  The packed weights and scales are the model's resident
+    which moves the activations in from pinned host memory, runs the layer
+    and moves the result out to pinned host memory, all inside the timed
+    region (for these page-locked, aligned buffers the transfers are the
+    library's zero-copy staging kernels).  The packed weights and scales are the model's resident
     parameters (rotated over the same copies as the device-timed loop, so
     they stream from HBM), not step inputs."""
     import torch

@@ -212,22 +212,29 @@ int nvfp4_linear_ex(const void* x, const uint8_t* w_packed, const uint8_t* w_sca
                     unsigned int flags, void* stream);
 
 /* nvfp4_linear_ex with the activations and the result in host memory:
- * enqueues on `stream` a copy of x_host into the caller's device buffer
- * x_dev, the layer (y_dev = x_dev . w^T as nvfp4_linear_ex), and a copy of
- * y_dev into y_host -- one cudaMemcpyAsync each way around the launch;
- * nothing is allocated.  (A convenience for callers whose activations live
- * in host memory; the operation is that of nvfp4_linear_ex.)
+ * enqueues on `stream` a transfer of x_host into the caller's device buffer
+ * x_dev, the layer (y_dev = x_dev . w^T as nvfp4_linear_ex), and a transfer
+ * of y_dev into y_host; nothing is allocated.  (A convenience for callers
+ * whose activations live in host memory; the operation is that of
+ * nvfp4_linear_ex.)
  *   x_host  host, bf16 [M, K] row-major;  x_dev  device, bf16 [M, K].
  *   y_dev   device, the output of nvfp4_linear_ex for `flags` (bf16, or
  *           fp32 with NVFP4_FLAG_F32_OUT; [M, N], or [M, N/2] with SWIGLU).
  *   y_host  host, same shape and type as y_dev.
- * For the copies to be asynchronous the host buffers must be page-locked
- * (cudaHostAlloc / cudaHostRegister); pageable buffers work, but the copies
- * then synchronise with the host.  The host buffers must stay valid, and
- * x_host unchanged, until the stream has passed the copies.  Validation and
- * errors as nvfp4_linear_ex (x_dev, y_dev in place of x, y; x_host and
- * y_host must not be NULL when M > 0); NVFP4_ERR_LAUNCH also when a copy
- * cannot be enqueued (an enqueued input copy is then left to complete). */
+ * Transfers: when both host buffers are page-locked and mapped into the
+ * device's address space (cudaHostAlloc, cudaHostRegister: every
+ * page-locked buffer under unified addressing) and all four buffers are
+ * 16-byte aligned, they are two small kernels that read x_host and write
+ * y_host directly over the host link (zero-copy), launched like the
+ * layer's own kernels as programmatic dependents, so that consecutive
+ * calls on a stream overlap (the next call's weights stream in while this
+ * one finishes).  Otherwise one cudaMemcpyAsync each way around the
+ * launch; pageable buffers then make the copies synchronise with the host.
+ * The host buffers must stay valid, and x_host unchanged, until the stream
+ * has passed the call.  Validation and errors as nvfp4_linear_ex (x_dev,
+ * y_dev in place of x, y; x_host and y_host must not be NULL when M > 0);
+ * NVFP4_ERR_LAUNCH also when a transfer cannot be enqueued (an enqueued
+ * input transfer is then left to complete). */
 int nvfp4_linear_host(const void* x_host, void* x_dev, const uint8_t* w_packed,
                       const uint8_t* w_scale, float global_scale, void* y_dev, void* y_host,
                       int64_t M, int64_t N, int64_t K, unsigned int flags, void* stream);

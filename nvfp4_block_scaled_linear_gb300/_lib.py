@@ -186,10 +186,11 @@ def linear_ex(x, w_packed, w_scale, global_scale, flags=0, out=None, stream=None
 
 def linear_host(x_host, x_dev, w_packed, w_scale, global_scale, y_dev, y_host, flags=0,
                 stream=None):
-    """Call nvfp4_linear_host: copy the host activations ``x_host`` into the
-    device buffer ``x_dev``, run the layer into ``y_dev`` and copy it to the
-    host tensor ``y_host``, all enqueued on ``stream`` (page-locked host
-    tensors keep the copies asynchronous).  Returns ``y_host``."""
+    """Call nvfp4_linear_host: move the host activations ``x_host`` into the
+    device buffer ``x_dev``, run the layer into ``y_dev`` and move it to the
+    host tensor ``y_host``, all enqueued on ``stream``.  Page-locked,
+    16-byte aligned host tensors take the zero-copy transfer kernels;
+    others are copied.  Returns ``y_host``."""
     w_packed, w_scale, M, N, K = _check(x_dev, w_packed, w_scale)
     n_out = N // 2 if flags & FLAG_SWIGLU else N
     dtype = torch.float32 if flags & FLAG_F32_OUT else torch.bfloat16

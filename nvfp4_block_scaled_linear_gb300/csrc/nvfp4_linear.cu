@@ -13,6 +13,7 @@
 #include "../../include/nvfp4_linear.h"
 #include "gemv_bf16.cuh"
 #include "gemv_tc.cuh"
+#include "host_io.cuh"
 #include "quantize.cuh"
 #include "smallm.cuh"
 #include "tcgemm.cuh"
@@ -848,6 +849,40 @@ unsigned resident_grid(Kernel kernel, int num_sms, int64_t units) {
       1, std::min<int64_t>(static_cast<int64_t>(num_sms) * per_sm, need)));
 }
 
+// The device address of a page-locked host buffer mapped into the current
+// device's address space, or nullptr (pageable memory, device memory).
+void* device_view(const void* host) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, host) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
+// One staging kernel of the host-buffer entry point, launched as a
+// programmatic dependent of the preceding kernel in the stream.
+int launch_staging(void (*kernel)(const uint4*, uint4*, int64_t), const uint4* src, uint4* dst,
+                   int64_t n, int num_sms, cudaStream_t stream) {
+  const int64_t need = (n + nvfp4::hostio::kThreads - 1) / nvfp4::hostio::kThreads;
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof cfg);
+  cfg.gridDim = dim3(static_cast<unsigned>(
+      std::max<int64_t>(1, std::min<int64_t>(need, static_cast<int64_t>(num_sms) * 4))));
+  cfg.blockDim = dim3(nvfp4::hostio::kThreads, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kernel, src, dst, n) != cudaSuccess) {
+    cudaGetLastError();
+    return NVFP4_ERR_LAUNCH;
+  }
+  return NVFP4_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -908,13 +943,41 @@ int nvfp4_linear_host(const void* x_host, void* x_dev, const uint8_t* w_packed,
   const int64_t n_out = (flags & NVFP4_FLAG_SWIGLU) ? N / 2 : N;
   const size_t y_bytes = static_cast<size_t>(M) * static_cast<size_t>(n_out) *
                          ((flags & NVFP4_FLAG_F32_OUT) ? 4 : 2);
-  if (cudaMemcpyAsync(x_dev, x_host, x_bytes, cudaMemcpyHostToDevice, stream) != cudaSuccess) {
+  // Page-locked host buffers mapped into the device's address space, all
+  // four buffers and both sizes 16-byte aligned: the transfers are kernels
+  // chained with the layer (zero-copy, see host_io.cuh); otherwise one
+  // cudaMemcpyAsync each way.
+  const void* xh = device_view(x_host);
+  void* yh = device_view(y_host);
+  const bool zero_copy = xh && yh &&
+                         ((reinterpret_cast<uintptr_t>(xh) | reinterpret_cast<uintptr_t>(yh) |
+                           reinterpret_cast<uintptr_t>(x_dev) |
+                           reinterpret_cast<uintptr_t>(y_dev) | x_bytes | y_bytes) &
+                          15u) == 0;
+  if (zero_copy) {
+    DeviceInfo* d = nullptr;
+    st = device_setup(&d);
+    if (st != NVFP4_OK) return st;
+    st = launch_staging(nvfp4::hostio::stage_in_kernel, static_cast<const uint4*>(xh),
+                        static_cast<uint4*>(x_dev), static_cast<int64_t>(x_bytes / 16),
+                        d->num_sms, stream);
+    if (st != NVFP4_OK) return st;
+  } else if (cudaMemcpyAsync(x_dev, x_host, x_bytes, cudaMemcpyHostToDevice, stream) !=
+             cudaSuccess) {
     cudaGetLastError();
     return NVFP4_ERR_LAUNCH;
   }
   st = run(x_dev, w_packed, w_scale, global_scale, global_scale, y_dev, M, N, K, flags,
            stream_ptr);
   if (st != NVFP4_OK) return st;
+  if (zero_copy) {
+    DeviceInfo* d = nullptr;
+    st = device_setup(&d);
+    if (st != NVFP4_OK) return st;
+    return launch_staging(nvfp4::hostio::stage_out_kernel, static_cast<const uint4*>(y_dev),
+                          static_cast<uint4*>(yh), static_cast<int64_t>(y_bytes / 16),
+                          d->num_sms, stream);
+  }
   if (cudaMemcpyAsync(y_host, y_dev, y_bytes, cudaMemcpyDeviceToHost, stream) != cudaSuccess) {
     cudaGetLastError();
     return NVFP4_ERR_LAUNCH;

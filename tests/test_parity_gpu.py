@@ -525,6 +525,55 @@ def test_host_buffer_call_equals_device_call(M, flags, pinned):
     assert torch.equal(dx.cpu().view(torch.int16), x.cpu().view(torch.int16))
 
 
+@pytest.mark.parametrize("M", [1, 40])
+def test_host_buffer_calls_chained_on_one_stream(M):
+    """Back-to-back nvfp4_linear_host calls on one stream sharing x_dev and
+    y_dev, each with its own page-locked input and output (the zero-copy
+    path, whose transfers are kernels chained by programmatic dependent
+    launch): every call reads its own activations and returns its own
+    result, bit for bit the device call's."""
+    n = 4
+    ts = [make_linear(M, 512, 1024, seed=3200 + 10 * M + i) for i in range(n)]
+    x0, wp, ws = to_dev(ts[0])
+    gs = float(ts[0].global_scale)
+    refs = []
+    hxs, hys = [], []
+    for t in ts:
+        x = torch.from_numpy(t.x_bits.view(np.int16)).view(torch.bfloat16)
+        refs.append(_lib.linear_ex(x.to(DEV), wp, ws, gs, 0).cpu())
+        hxs.append(x.clone().pin_memory())
+        hys.append(torch.full((M, 512), float("nan"), dtype=torch.bfloat16).pin_memory())
+    dx = torch.empty_like(x0)
+    dy = torch.empty((M, 512), dtype=torch.bfloat16, device=DEV)
+    s = torch.cuda.Stream()
+    for rep in range(3):
+        for i in range(n):
+            _lib.linear_host(hxs[i], dx, wp, ws, gs, dy, hys[i], 0, stream=s)
+    s.synchronize()
+    for i in range(n):
+        assert torch.equal(hys[i].view(torch.int16), refs[i].view(torch.int16)), "call %d" % i
+
+
+def test_host_buffers_off_16_byte_alignment_take_the_copies():
+    """Page-locked buffers 2 bytes into their allocation cannot take the
+    16-byte staging kernels: the call copies instead, same result."""
+    M, N, K = 3, 512, 1024
+    t = make_linear(M, N, K, seed=3300)
+    x, wp, ws = to_dev(t)
+    ref = _lib.linear_ex(x, wp, ws, float(t.global_scale), 0).cpu()
+    big_x = torch.empty(M * K + 8, dtype=torch.bfloat16).pin_memory()
+    big_y = torch.empty(M * N + 8, dtype=torch.bfloat16).pin_memory()
+    hx = big_x[1:1 + M * K].view(M, K)
+    hy = big_y[1:1 + M * N].view(M, N)
+    hx.copy_(x.cpu())
+    dx = torch.empty_like(x)
+    dy = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
+    s = torch.cuda.Stream()
+    _lib.linear_host(hx, dx, wp, ws, float(t.global_scale), dy, hy, 0, stream=s)
+    s.synchronize()
+    assert torch.equal(hy.view(torch.int16), ref.view(torch.int16))
+
+
 def test_cuda_graph_capture_and_replay():
     """Calls captured into a CUDA graph (both kernels, SwiGLU and plain)
     give on replay what the same calls give eagerly, bit for bit, also after
