@@ -374,8 +374,8 @@ def quantize_case(lib, dev, stream, hbm_peak, N=34816, K=5120, steps=20):
     """The load-time quantiser (bf16 -> NVFP4) on the decode projection's
     weight shape: bytes = bf16 in + codes + scales out (HBM-bound)."""
     import torch
-    g = torch.Generator(device="cpu").manual_seed(11)
-    w = (torch.randn((N, K), generator=g) * 0.02).to(torch.bfloat16).to(dev)
+    from nvfp4_block_scaled_linear_gb300.inputs import quantizer_weight
+    w = quantizer_weight(N, K).to(dev)
     with torch.cuda.stream(stream):
         for _ in range(3):
             lib.quantize(w, stream=stream)
@@ -400,10 +400,9 @@ def quantize_fp8_case(lib, dev, stream, hbm_peak, N=34816, K=5120, block=128, st
     """The load-time FP8 -> NVFP4 conversion on the same weight shape:
     bytes = e4m3 codes and block scales in + codes + scales out."""
     import torch
-    g = torch.Generator(device="cpu").manual_seed(12)
-    w8 = (torch.randn((N, K), generator=g) * 60.0).to(torch.float8_e4m3fn).to(dev)
-    sinv = torch.exp(torch.empty((-(-N // block), -(-K // block))).uniform_(-9, 2, generator=g)) \
-        .to(dev)
+    from nvfp4_block_scaled_linear_gb300.inputs import fp8_checkpoint_tensor
+    w8, sinv = fp8_checkpoint_tensor(N, K, block)
+    w8, sinv = w8.to(dev), sinv.to(dev)
     with torch.cuda.stream(stream):
         for _ in range(3):
             lib.quantize_fp8(w8, sinv, block, stream=stream)

@@ -133,6 +133,25 @@ WORKLOADS = {
 }
 
 
+# The load-time quantisers' inputs, on the decode gate+up weight shape: a
+# bf16 weight of N(0, 0.02^2) values, and a block-scaled FP8 checkpoint
+# tensor (e4m3 codes of N(0, 60^2) values by torch's round-to-nearest
+# conversion -- values past 448 would become NaN codes, a 7.5-sigma event
+# absent from these draws -- and one fp32 scale_inv per 128 x 128 tile,
+# exp(U(-9, 2))).  CPU tensors, drawn from torch.Generator(seed).
+def quantizer_weight(N: int = 34816, K: int = 5120, seed: int = 11) -> torch.Tensor:
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    return (torch.randn((N, K), generator=g) * 0.02).to(torch.bfloat16)
+
+
+def fp8_checkpoint_tensor(N: int = 34816, K: int = 5120, block: int = 128, seed: int = 12):
+    """(w8 float8_e4m3fn [N, K], scale_inv float32 [ceil(N/block), ceil(K/block)])."""
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    w8 = (torch.randn((N, K), generator=g) * 60.0).to(torch.float8_e4m3fn)
+    sinv = torch.exp(torch.empty((-(-N // block), -(-K // block))).uniform_(-9, 2, generator=g))
+    return w8, sinv
+
+
 def algorithmic_bytes(M: int, N: int, K: int, swiglu: bool = False) -> int:
     """Bytes the layer must move: packed weights and scales once, x once,
     y once (bf16), the global scale once."""

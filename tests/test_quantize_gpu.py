@@ -177,3 +177,45 @@ def test_quantize_fp8_equals_bf16_quantiser_on_the_converted_tensor():
     torch.cuda.synchronize()
     for x, y in zip(a, b):
         assert torch.equal(x, y)
+
+
+# ------------------------------------------------------------------ full size
+def _sampled_rows(row_absmax, rng, count=509):
+    """Random rows plus the first, the last and the one holding the tensor's
+    largest magnitude (so that the global scale over the sample is the
+    tensor's)."""
+    N = row_absmax.shape[0]
+    extra = [0, N - 1, int(np.argmax(row_absmax))]
+    return np.unique(np.concatenate([rng.choice(N, count, replace=False), extra]))
+
+
+def test_quantizers_at_the_benchmarked_size_on_sampled_rows():
+    """The bench's quantiser inputs (34816 x 5120: the bf16 weight and the
+    block-scaled FP8 tensor), checked bit for bit on sampled rows.  Rows
+    quantise independently given the global scale, and the sample holds the
+    row with the largest |w| (for FP8, the largest |bf16 image|), so the
+    oracle's global scale over the sample is the whole tensor's."""
+    from nvfp4_block_scaled_linear_gb300.inputs import fp8_checkpoint_tensor, quantizer_weight
+    rng = np.random.default_rng(77)
+    w = quantizer_weight()
+    wp, ws, gs = _lib.quantize(w.to(DEV))
+    torch.cuda.synchronize()
+    rows = _sampled_rows(w.float().abs().amax(1).numpy(), rng)
+    wp_o, ws_o, gs_o = oracle.quantize(w.view(torch.int16).numpy().view(np.uint16)[rows])
+    assert np.float32(gs.cpu().numpy()[0]) == gs_o
+    assert np.array_equal(ws.cpu().numpy()[rows], ws_o)
+    assert np.array_equal(wp.cpu().numpy()[rows], wp_o)
+    del w, wp, ws
+
+    w8, sinv = fp8_checkpoint_tensor()
+    w8_bits = w8.view(torch.uint8).numpy()
+    assert not ((w8_bits & 0x7F) == 0x7F).any()          # no NaN codes in the draw
+    wp, ws, gs = _lib.quantize_fp8(w8.to(DEV), sinv.to(DEV), 128)
+    torch.cuda.synchronize()
+    img = oracle.fp8_to_bf16(w8_bits, sinv.numpy(), 128)
+    img_absmax = torch.from_numpy(img.view(np.int16)).view(torch.bfloat16).float().abs().amax(1)
+    rows = _sampled_rows(img_absmax.numpy(), rng)
+    wp_o, ws_o, gs_o = oracle.quantize(img[rows])
+    assert np.float32(gs.cpu().numpy()[0]) == gs_o
+    assert np.array_equal(ws.cpu().numpy()[rows], ws_o)
+    assert np.array_equal(wp.cpu().numpy()[rows], wp_o)
