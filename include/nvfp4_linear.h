@@ -224,12 +224,14 @@ int nvfp4_linear_ex(const void* x, const uint8_t* w_packed, const uint8_t* w_sca
  * Transfers: when both host buffers are page-locked and mapped into the
  * device's address space (cudaHostAlloc, cudaHostRegister: every
  * page-locked buffer under unified addressing) and all four buffers are
- * 16-byte aligned, they are two small kernels that read x_host and write
- * y_host directly over the host link (zero-copy), launched like the
- * layer's own kernels as programmatic dependents, so that consecutive
- * calls on a stream overlap (the next call's weights stream in while this
- * one finishes).  Otherwise one cudaMemcpyAsync each way around the
- * launch; pageable buffers then make the copies synchronise with the host.
+ * 16-byte aligned, they go directly over the host link (zero-copy): a small
+ * kernel reads x_host into x_dev, and the layer's kernel writes its result
+ * to y_host as well as y_dev from its epilogue (M <= 32; for M > 32 a
+ * second small kernel copies y_dev to y_host).  All are launched like the
+ * layer's own kernels as programmatic dependents, so that consecutive calls
+ * on a stream overlap (the next call's weights stream in while this one
+ * finishes).  Otherwise one cudaMemcpyAsync each way around the launch;
+ * pageable buffers then make the copies synchronise with the host.
  * The host buffers must stay valid, and x_host unchanged, until the stream
  * has passed the call.  Validation and errors as nvfp4_linear_ex (x_dev,
  * y_dev in place of x, y; x_host and y_host must not be NULL when M > 0);

@@ -118,6 +118,8 @@ __host__ __device__ constexpr bool layout_ok(const SmemLayout& l, int n_mma) {
 
 struct Params {
   void* y;              // [M, N] (or [M, N/2] with swiglu), bf16 or f32
+  void* y_host;         // nullptr, or the same output again in host memory mapped
+                        // into the device (the host-buffer entry point)
   int64_t M, N, K;
   float out_scale;      // 1 / global_scale
   float out_scale_up;   // 1 / the up rows' global scale (SwiGLU)
@@ -529,10 +531,14 @@ __global__ void __launch_bounds__(Roles<NM>::kThreads, NM == 16 ? 2 : 1)
       float yv = v * (p.seg.n ? seg_scale(p.seg, n_base + j) : p.out_scale);
       if (p.swiglu) yv = silu_mul(yv, u * p.out_scale_up);
       const int64_t off = static_cast<int64_t>(m) * n_out + n_base + j;
-      if (p.out_f32)
+      if (p.out_f32) {
         static_cast<float*>(p.y)[off] = yv;
-      else
-        static_cast<__nv_bfloat16*>(p.y)[off] = __float2bfloat16_rn(yv);
+        if (p.y_host) static_cast<float*>(p.y_host)[off] = yv;
+      } else {
+        const __nv_bfloat16 yb = __float2bfloat16_rn(yv);
+        static_cast<__nv_bfloat16*>(p.y)[off] = yb;
+        if (p.y_host) static_cast<__nv_bfloat16*>(p.y_host)[off] = yb;
+      }
     }
   }
   if (split > 1) {

@@ -3,10 +3,11 @@
 // On GB300 page-locked host memory sits in the GPU's address space over the
 // coherent NVLink-C2C link, so a kernel can read the activations from, and
 // write the result to, the caller's host buffers directly (zero-copy).  As
-// kernels, the two transfers join the chain of programmatic dependent
-// launches the layer's kernels already form: consecutive calls on a stream
-// then overlap the next call's weight prefetch with the current call, which a
-// copy-engine transfer between two kernels prevents.
+// kernels (or, for a few-row kernel's result, as part of its epilogue), the
+// transfers join the chain of programmatic dependent launches the layer's
+// kernels already form: consecutive calls on a stream then overlap the next
+// call's weight prefetch with the current call, which a copy-engine transfer
+// between two kernels prevents.
 //
 // Ordering (every launch of the chain carries programmatic stream
 // serialisation; griddepcontrol.wait waits for the whole preceding grid,
@@ -14,8 +15,11 @@
 //   stage_in   reads the host activations before its wait (nothing on the
 //              device writes them), writes x_dev after it (the preceding
 //              call may still read x_dev);
-//   the layer  reads x_dev after its wait;
-//   stage_out  reads y_dev and writes the host result after its wait.
+//   the layer  reads x_dev after its wait; the few-row kernels (M <= 32)
+//              write the result to y_dev and, from the same epilogue, to
+//              the host buffer;
+//   stage_out  (M > 32 only) reads y_dev and writes the host result after
+//              its wait.
 #pragma once
 #include <cstdint>
 

@@ -455,7 +455,8 @@ SmallmPlan plan_smallm(const DeviceInfo& d, int64_t M, int64_t N, int64_t K,
 template <int MT, int CV>
 int launch_smallm(const DeviceInfo& d, const void* x, const uint8_t* wp, const uint8_t* ws,
                   float gs, float gs_up, void* y, int64_t M, int64_t N, int64_t K, unsigned int flags,
-                  cudaStream_t stream, const SegSpec* segs) {
+                  cudaStream_t stream, const SegSpec* segs,
+                  void* y_host) {
   constexpr bool F16 = CV > 0;
   const bool swiglu = flags & NVFP4_FLAG_SWIGLU;
   static PlanMemo<SmallmPlan> memo;
@@ -478,6 +479,7 @@ int launch_smallm(const DeviceInfo& d, const void* x, const uint8_t* wp, const u
 
   sm::Params p;
   p.y = y;
+  p.y_host = y_host;
   p.M = M;
   p.N = N;
   p.K = K;
@@ -577,7 +579,8 @@ GemvPlan plan_gemv(const DeviceInfo& d, int64_t M, int64_t N, int64_t K, unsigne
 template <int NM>
 int launch_gemv(const DeviceInfo& d, const void* x, const uint8_t* wp, const uint8_t* ws,
                 float gs, float gs_up, void* y, int64_t M, int64_t N, int64_t K, unsigned int flags,
-                cudaStream_t stream, const SegSpec* segs) {
+                cudaStream_t stream, const SegSpec* segs,
+                  void* y_host) {
   static PlanMemo<GemvPlan> memo;
   const GemvPlan plan =
       memo.get(d, M, N, K, flags, [&] { return plan_gemv<NM>(d, M, N, K, flags); });
@@ -592,6 +595,7 @@ int launch_gemv(const DeviceInfo& d, const void* x, const uint8_t* wp, const uin
     return NVFP4_ERR_LAUNCH;
   gt::Params p;
   p.y = y;
+  p.y_host = y_host;
   p.M = M;
   p.N = N;
   p.K = K;
@@ -680,7 +684,8 @@ GemvBfPlan plan_gemv_bf16(const DeviceInfo& d, int64_t N, int64_t K, unsigned in
 template <int NM, int NI>
 int launch_gemv_bf16(const DeviceInfo& d, const void* x, const uint8_t* wp, const uint8_t* ws,
                      float gs, float gs_up, void* y, int64_t M, int64_t N, int64_t K,
-                     unsigned int flags, cudaStream_t stream, const SegSpec* segs) {
+                     unsigned int flags, cudaStream_t stream, const SegSpec* segs,
+                  void* y_host) {
   static PlanMemo<GemvBfPlan> memo;
   const GemvBfPlan plan =
       memo.get(d, 0, N, K, flags, [&] { return plan_gemv_bf16<NM, NI>(d, N, K, flags); });
@@ -695,6 +700,7 @@ int launch_gemv_bf16(const DeviceInfo& d, const void* x, const uint8_t* wp, cons
     return NVFP4_ERR_LAUNCH;
   gb::Params p;
   p.y = y;
+  p.y_host = y_host;
   p.M = M;
   p.N = N;
   p.K = K;
@@ -736,13 +742,14 @@ int launch_gemv_bf16(const DeviceInfo& d, const void* x, const uint8_t* wp, cons
 template <int NM>
 int launch_gemv_bf16_any(const DeviceInfo& d, const void* x, const uint8_t* wp,
                          const uint8_t* ws, float gs, float gs_up, void* y, int64_t M, int64_t N,
-                         int64_t K, unsigned int flags, cudaStream_t stream, const SegSpec* segs) {
+                         int64_t K, unsigned int flags, cudaStream_t stream, const SegSpec* segs,
+                  void* y_host) {
   int want = (flags & NVFP4_FLAG_GROUPS_MASK) >> NVFP4_FLAG_GROUPS_SHIFT;
   if (want != 0 && want != 2 && want != 4) return NVFP4_ERR_INVALID;
   if (want == 0) want = N / gb::kRows >= d.num_sms ? 2 : 4;
   if (want == 2)
-    return launch_gemv_bf16<NM, 2>(d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs);
-  return launch_gemv_bf16<NM, 4>(d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs);
+    return launch_gemv_bf16<NM, 2>(d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs, y_host);
+  return launch_gemv_bf16<NM, 4>(d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs, y_host);
 }
 
 int launch_tcgemm(const DeviceInfo& d, const void* x, const uint8_t* wp, const uint8_t* ws,
@@ -794,9 +801,11 @@ int launch_tcgemm(const DeviceInfo& d, const void* x, const uint8_t* wp, const u
   return NVFP4_OK;
 }
 
+// y_host (few-row kernels only): a second copy of the output, written by the
+// kernel's epilogue into host memory mapped into the device.
 int run(const void* x, const uint8_t* wp, const uint8_t* ws, float gs, float gs_up, void* y,
         int64_t M, int64_t N, int64_t K, unsigned int flags, void* stream_ptr,
-        const SegSpec* segs = nullptr) {
+        const SegSpec* segs = nullptr, void* y_host = nullptr) {
   int st = validate(x, wp, ws, y, M, N, K, flags);
   if (st != NVFP4_OK) return st;
   if (M == 0) return NVFP4_OK;
@@ -807,12 +816,12 @@ int run(const void* x, const uint8_t* wp, const uint8_t* ws, float gs, float gs_
   const int kernel = kernel_for(M, N, K, flags);
   if (kernel == NVFP4_KERNEL_GEMV_BF16) {
     if (M <= 16)
-      return launch_gemv_bf16_any<16>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs);
-    return launch_gemv_bf16_any<32>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs);
+      return launch_gemv_bf16_any<16>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs, y_host);
+    return launch_gemv_bf16_any<32>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs, y_host);
   }
   if (kernel == NVFP4_KERNEL_GEMV) {
-    if (M <= 16) return launch_gemv<16>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs);
-    return launch_gemv<32>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs);
+    if (M <= 16) return launch_gemv<16>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs, y_host);
+    return launch_gemv<32>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs, y_host);
   }
   if (kernel == NVFP4_KERNEL_SMALLM) {
     switch ((M + 7) / 8) {
@@ -821,15 +830,18 @@ int run(const void* x, const uint8_t* wp, const uint8_t* ws, float gs, float gs_
         // (verify, M = 7: 19.5 us against 22.4 with one; M = 5: 18.4
         // against 19.6; decode, M = 1: 21.8 against 22.4 with two)
         if (flags & NVFP4_FLAG_BF16_MMA)
-          return launch_smallm<1, 0>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs);
+          return launch_smallm<1, 0>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs, y_host);
         if (M <= 3)
-          return launch_smallm<1, 1>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs);
-        return launch_smallm<1, 2>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs);
-      case 2: return launch_smallm<2, 0>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs);
-      case 3: return launch_smallm<3, 0>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs);
-      default: return launch_smallm<4, 0>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs);
+          return launch_smallm<1, 1>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs, y_host);
+        return launch_smallm<1, 2>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs, y_host);
+      case 2: return launch_smallm<2, 0>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs, y_host);
+      case 3: return launch_smallm<3, 0>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs, y_host);
+      default: return launch_smallm<4, 0>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs, y_host);
     }
   }
+  // (the tensor-core kernel writes no second output: a large M's result goes
+  // to host memory after the kernel, not from its epilogue)
+  if (y_host) return NVFP4_ERR_INVALID;
   return launch_tcgemm(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs);
 }
 
@@ -954,8 +966,8 @@ int nvfp4_linear_host(const void* x_host, void* x_dev, const uint8_t* w_packed,
                            reinterpret_cast<uintptr_t>(x_dev) |
                            reinterpret_cast<uintptr_t>(y_dev) | x_bytes | y_bytes) &
                           15u) == 0;
+  DeviceInfo* d = nullptr;
   if (zero_copy) {
-    DeviceInfo* d = nullptr;
     st = device_setup(&d);
     if (st != NVFP4_OK) return st;
     st = launch_staging(nvfp4::hostio::stage_in_kernel, static_cast<const uint4*>(xh),
@@ -967,17 +979,18 @@ int nvfp4_linear_host(const void* x_host, void* x_dev, const uint8_t* w_packed,
     cudaGetLastError();
     return NVFP4_ERR_LAUNCH;
   }
+  // The few-row kernels (M <= 32) also write the result straight into the
+  // mapped host buffer from their epilogue; the tensor-core kernel's output
+  // is moved by the output staging kernel.
+  const bool mirror = zero_copy && kernel_for(M, N, K, flags) != NVFP4_KERNEL_TCGEMM;
   st = run(x_dev, w_packed, w_scale, global_scale, global_scale, y_dev, M, N, K, flags,
-           stream_ptr);
+           stream_ptr, nullptr, mirror ? yh : nullptr);
   if (st != NVFP4_OK) return st;
-  if (zero_copy) {
-    DeviceInfo* d = nullptr;
-    st = device_setup(&d);
-    if (st != NVFP4_OK) return st;
+  if (mirror) return NVFP4_OK;
+  if (zero_copy)
     return launch_staging(nvfp4::hostio::stage_out_kernel, static_cast<const uint4*>(y_dev),
                           static_cast<uint4*>(yh), static_cast<int64_t>(y_bytes / 16),
                           d->num_sms, stream);
-  }
   if (cudaMemcpyAsync(y_host, y_dev, y_bytes, cudaMemcpyDeviceToHost, stream) != cudaSuccess) {
     cudaGetLastError();
     return NVFP4_ERR_LAUNCH;

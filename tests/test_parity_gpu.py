@@ -503,11 +503,17 @@ def test_concurrent_calls_from_two_threads_on_two_streams():
     assert not failures, failures
 
 
-@pytest.mark.parametrize("M,flags,pinned", [(1, 0, True), (7, _lib.FLAG_SWIGLU, True),
-                                            (20, _lib.FLAG_F32_OUT, False), (40, 0, True)])
+@pytest.mark.parametrize("M,flags,pinned", [
+    (1, 0, True), (7, _lib.FLAG_SWIGLU, True), (20, _lib.FLAG_F32_OUT, False),
+    (20, _lib.FLAG_F32_OUT, True), (12, _lib.FLAG_SWIGLU | _lib.FLAG_F32_OUT, True),
+    (20, _lib.FLAG_FORCE_GEMV | _lib.FLAG_BF16_MMA, True), (12, _lib.FLAG_FORCE_GEMV, True),
+    (40, 0, True)])
 def test_host_buffer_call_equals_device_call(M, flags, pinned):
     """nvfp4_linear_host (activations and result in host memory, page-locked
-    or not) gives the device call's output bit for bit."""
+    or not) gives the device call's output bit for bit: with page-locked
+    buffers each few-row kernel (the warp-MMA kernel in f16 and bf16, both
+    tcgen05 few-row kernels) also writes the result into the host buffer from
+    its epilogue, and at M > 32 the output staging kernel moves it."""
     t = make_linear(M, 512, 1024, seed=3100 + M)
     x, wp, ws = to_dev(t)
     ref = _lib.linear_ex(x, wp, ws, float(t.global_scale), flags).cpu()
