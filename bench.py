@@ -16,7 +16,7 @@ weights from HBM.
 The other workloads (verify, M=32 layer, prefill with and without SwiGLU)
 are timed the same way and reported under "workloads".
 
---impl reference times the CPU oracle (the reference arm of this build) on
+--impl reference times the CPU oracle (the reference arm) on
 the host cores, on a bounded sample of the same workload per step.
 
 Multi-GPU (torchrun): every rank runs an independent replica on its own GPU
