@@ -230,8 +230,11 @@ int nvfp4_linear_ex(const void* x, const uint8_t* w_packed, const uint8_t* w_sca
  * second small kernel copies y_dev to y_host).  All are launched like the
  * layer's own kernels as programmatic dependents, so that consecutive calls
  * on a stream overlap (the next call's weights stream in while this one
- * finishes).  Otherwise one cudaMemcpyAsync each way around the launch;
- * pageable buffers then make the copies synchronise with the host.
+ * finishes).  The input stage reads x_host before the kernel ahead of it in
+ * the stream has completed (as the layer does with its weights), so x_host
+ * must not be written by that kernel.  Otherwise one cudaMemcpyAsync each
+ * way around the launch; pageable buffers then make the copies synchronise
+ * with the host.
  * The host buffers must stay valid, and x_host unchanged, until the stream
  * has passed the call.  Validation and errors as nvfp4_linear_ex (x_dev,
  * y_dev in place of x, y; x_host and y_host must not be NULL when M > 0);
