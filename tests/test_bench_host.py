@@ -57,3 +57,18 @@ def test_reference_arm_other_ranks_exit_silently():
            "--workload", "tiny", "--steps", "3", "--warmup", "3"]
     r = subprocess.run(cmd, capture_output=True, text=True, timeout=300, cwd=ROOT, env=env)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_traffic_is_reported_only_for_the_profiled_sources(monkeypatch):
+    """roofline.traffic comes from the committed ncu summary only while the
+    kernel sources hash to what the capture recorded; any other hash (the
+    sources changed since) turns it into null."""
+    with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+        recorded = json.load(f)["smallm"]["decode_gate_up"]["source_hash"]
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: recorded)
+    v = bench.profiled_traffic("smallm", "decode_gate_up")
+    assert v is not None and 0.9 * 100_349_956 < v < 1.2 * 100_349_956
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: "0" * 16)
+    assert bench.profiled_traffic("smallm", "decode_gate_up") is None
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda: recorded)
+    assert bench.profiled_traffic("no_such_kernel", "decode_gate_up") is None
