@@ -181,6 +181,21 @@ def whole_job_value(units_per_rank, max_seconds, world):
     return units_per_rank * world / max_seconds
 
 
+def workload_config(name, linears, swiglu):
+    """The `config` of the JSON line: the workload alone (its name, shapes and
+    epilogue), identical in both arms; measurement notes go elsewhere."""
+    return {"workload": name, "shapes": [[int(t.M), int(t.N), int(t.K)] for t in linears],
+            "swiglu": bool(swiglu)}
+
+
+def compute_dtype(kernel, M):
+    """The arithmetic the launched kernel multiplies in (fp32 accumulation in
+    every kernel): the warp-MMA kernel at M <= 8 multiplies f16 operands (exact
+    code * scale, activations scaled by a power of two; bf16 for a row's stage
+    beyond the f16 window), every other path bf16."""
+    return "f16" if kernel == "smallm" and M <= 8 else "bf16"
+
+
 # ----------------------------------------------------------------- GPU arm
 class Case:
     """Device-resident inputs of one workload, with rotated weight copies."""
@@ -470,18 +485,19 @@ def run_ours(args):
     line = {"metric": METRIC, "value": round(value, 2), "unit": unit, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(max_step_s * 1e3, 6), "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": compute_dtype(head.kernel, head.linears[0].M),
             "data": "synthetic (seeded; checkpoint-schema layouts, random codes/scales/"
                     "activations)",
-            "config": {"workload": head.name, "shapes": [[t.M, t.N, t.K] for t in head.linears],
-                       "swiglu": head.w.swiglu, "l2": head.l2_note(),
-                       "parallelism": "replicas" if world > 1 else "single GPU"},
+            "config": workload_config(head.name, head.linears, head.w.swiglu),
+            "l2": head.l2_note(),
+            "parallelism": "replicas" if world > 1 else "single GPU",
             "roofline": roofline, "gpu_launches": args.steps * head.launches_per_step,
             "timing": ("CUDA graphs of consecutive steps, CUDA events on the launching "
                        "stream around the replays" if not args.eager else
                        "eager launches, CUDA events around each launch")}
     if args.max_rows is not None:
-        line["config"]["max_rows"] = args.max_rows
+        line["max_rows"] = args.max_rows
 
     if not args.no_extras:
         e2e_ms, h2d, d2h = e2e_case(head, max(3, min(500, args.steps)), stream, dev)
@@ -498,6 +514,7 @@ def run_ours(args):
             tot, lms = time_case(c, steps, 5, stream, world, sampler, graph=not args.eager)
             ms = tot / steps
             ent = {"ms_per_step": round(ms, 5), "kernel": c.kernel,
+                   "dtype": compute_dtype(c.kernel, c.linears[0].M),
                    "launch_us": [round(v * 1e3, 2) for v in lms]}
             if c.linears[0].M > 32:
                 tf = c.flops / (ms / 1e3) / 1e12
@@ -576,6 +593,39 @@ def _cpu_model():
     return platform.processor() or platform.machine()
 
 
+# Oracle timing per configuration: every output on all cores; on one core,
+# every output for the small configurations and a labelled prefix of the
+# activation rows (time scaled by M / rows) for the M = 32 layer and prefill,
+# whose full oracle takes minutes there.
+ORACLE_TIMING_ROWS = {"layer_m32": (32, 4), "prefill": (16, 2)}   # (all cores, one core)
+
+
+def oracle_timings(threads):
+    import oracle
+    from nvfp4_block_scaled_linear_gb300.inputs import WORKLOADS
+    out = {}
+    for name in ("tiny", "decode_gate_up", "verify_down", "layer_m32", "prefill"):
+        linears = WORKLOADS[name].draw()
+        ent = {}
+        for label, thr, pick in (("all_cores", threads, 0), ("one_core", 1, 1)):
+            total, notes = 0.0, []
+            for t in linears:
+                rows = min(t.M, ORACLE_TIMING_ROWS.get(name, (t.M, t.M))[pick])
+                t0 = time.perf_counter()
+                oracle.linear_f64(t.x_bits[:rows], t.w_packed, t.w_scale, t.global_scale,
+                                  threads=thr)
+                el = time.perf_counter() - t0
+                total += el * t.M / rows
+                if rows < t.M:
+                    notes.append("%s: rows [0,%d) of %d, time x %g" % (t.name, rows, t.M,
+                                                                        t.M / rows))
+            ent[label] = {"ms": round(total * 1e3, 2), "threads": thr,
+                          "sample": "; ".join(notes) if notes else "every output"}
+        out[name] = ent
+        del linears
+    return out
+
+
 def cpu_baseline(case, budget_s=10.0):
     """The oracle, as it stands, on the host cores (all of them, and one):
     repeated passes over a row sample of the headline workload for about
@@ -591,7 +641,8 @@ def cpu_baseline(case, budget_s=10.0):
                 done, n_rows, case.name, t.M, t.K, el),
             "one_core": {"value": round(value1, 4), "sample": "%d passes over rows [0,%d), %.1f s"
                          % (done1, n_rows1, el1)},
-            "cpu": _cpu_model()}
+            "cpu": _cpu_model(),
+            "oracle_ms_per_workload": oracle_timings(threads)}
 
 
 def run_reference(args):
@@ -601,7 +652,8 @@ def run_reference(args):
     import oracle
     from nvfp4_block_scaled_linear_gb300.inputs import WORKLOADS, algorithmic_bytes, flops
     w = WORKLOADS[args.workload]
-    t = w.draw()[0]
+    linears = w.draw()
+    t = linears[0]
     threads = oracle.default_threads()
     # Size one step so that warmup + steps end within ~2 minutes.
     probe_rows = min(t.N, 512)
@@ -636,7 +688,7 @@ def run_reference(args):
             "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded)",
-            "config": {"workload": w.name, "shapes": [[t.M, t.N, t.K]], "swiglu": w.swiglu},
+            "config": workload_config(w.name, linears, w.swiglu),
             "cpu_baseline": {"value": round(value, 6), "unit": unit, "cores": threads,
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": round(value, 6), "unit": unit, "h2d_bytes_per_step": 0,

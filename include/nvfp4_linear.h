@@ -84,21 +84,32 @@ extern "C" {
 #define NVFP4_FLAG_GROUPS_SHIFT 13
 #define NVFP4_FLAG_GROUPS_MASK (0xFu << NVFP4_FLAG_GROUPS_SHIFT)
 #define NVFP4_FLAG_GROUPS(n) (((unsigned int)(n) & 0xFu) << NVFP4_FLAG_GROUPS_SHIFT)
-/* Multiply in bf16, the activations as given (exact for any activations;
- * M <= 32): at M <= 8 the warp-MMA few-row kernel in bf16 instead of f16;
- * with NVFP4_FLAG_FORCE_GEMV the bf16 tcgen05 few-row kernel.  (Every
- * default for M = 9..32 is already bf16: the bf16 tcgen05 kernel on weight
- * matrices of N * K >= 2^26, the warp-MMA kernel otherwise.)  Without it,
- * M <= 8 multiplies in f16: code * scale is exact in f16, and each
- * activation row is brought to f16 after scaling by a power of two taken
- * from the row's running maximum |x|, which is exact for every activation
- * within a factor 2^31 of that maximum and otherwise rounds it like an f16
- * subnormal.  The f16 tcgen05 few-row kernel (only when forced) does the
- * same with the maximum within each 256-k stage. */
+/* Multiply in bf16, the activations as given (M <= 32): at M <= 8 the
+ * warp-MMA few-row kernel in bf16 instead of f16; with NVFP4_FLAG_FORCE_GEMV
+ * the bf16 tcgen05 few-row kernel.  (Every default for M = 9..32 is already
+ * bf16: the bf16 tcgen05 kernel on weight matrices of N * K >= 2^26, the
+ * warp-MMA kernel otherwise.)  Without it, M <= 8 multiplies in f16: code *
+ * scale is exact in f16, and each activation row is brought to f16 after
+ * scaling by a power of two taken from the row's running maximum |x|, which
+ * is exact for every activation within a factor 2^31 of that maximum; a
+ * 256-k stage of a row holding a nonzero value below that window is
+ * multiplied in bf16 instead, so the default is exact for every finite bf16
+ * activation as well.  The f16 tcgen05 few-row kernel (only when forced)
+ * scales by the maximum within each 256-k stage and has no such fallback:
+ * there an activation more than 2^31 below its stage's maximum rounds like
+ * an f16 subnormal. */
 #define NVFP4_FLAG_BF16_MMA (1u << 17)
 /* Force a tcgen05 few-row kernel (needs M <= 32): the f16 one, or with
  * NVFP4_FLAG_BF16_MMA the bf16 one. */
 #define NVFP4_FLAG_FORCE_GEMV (1u << 18)
+/* Test hook of the wait limit (see nvfp4_device_status): the warp-MMA
+ * few-row kernel never loads its last k stage and gives each pipeline wait a
+ * 1 ms limit, so the waits for that stage run out.  The call still returns
+ * and its kernel completes, with bit 0 of the device error word set and the
+ * output undefined.  Accepted only together with NVFP4_FLAG_FORCE_SMALLM and
+ * NVFP4_FLAG_SPLIT(1) (no thread-block cluster, no TMEM); otherwise
+ * NVFP4_ERR_INVALID.  Not for production calls. */
+#define NVFP4_FLAG_TEST_STALL (1u << 19)
 
 /* Kernel identifiers returned by nvfp4_linear_kernel_for. */
 #define NVFP4_KERNEL_NONE 0
@@ -251,7 +262,9 @@ int nvfp4_linear_kernel_for(int64_t M, int64_t N, int64_t K, unsigned int flags)
 
 /* Read the current device's error word (OR of bits set by kernels since it
  * was last cleared: bit 0 = a pipeline wait timed out) into *bits; clear it
- * if `clear` is non-zero.  Synchronises with the device.  Returns a status. */
+ * if `clear` is non-zero.  Synchronises with the whole device (every stream)
+ * first; the read and the clear are one atomic step on the device, so a bit
+ * set meanwhile is never lost.  Returns a status. */
 int nvfp4_device_status(unsigned int* bits, int clear);
 
 #ifdef __cplusplus

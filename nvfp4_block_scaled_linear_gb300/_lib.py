@@ -22,6 +22,7 @@ FLAG_FORCE_SMALLM = 4
 FLAG_FORCE_TCGEMM = 8
 FLAG_BF16_MMA = 1 << 17
 FLAG_FORCE_GEMV = 1 << 18
+FLAG_TEST_STALL = 1 << 19       # test hook of the wait limit (see the header)
 
 
 def FLAG_SPLIT(n):

@@ -51,10 +51,18 @@ __device__ __forceinline__ float seg_scale(const SegScales& s, int64_t col) {
   return sc;
 }
 
-// SwiGLU epilogue: silu(g) * u = g / (1 + e^-g) * u, in fp32 with the CUDA
-// fast exponential and fast division (a few ulp; e^-g = inf gives 0).
+// SwiGLU epilogue: silu(g) * u = g / (1 + e^-g) * u in fp32, written with
+// t = e^-|g| so that nothing overflows: g / (1 + t) for g >= 0, and
+// g * t / (1 + t) -- the same number -- for g < 0.  t comes from the CUDA fast
+// exponential (a few ulp here) and the division is the fast one, exact to a
+// few ulp for a denominator in [1, 2].  The fast exponential flushes results
+// below fp32's normal range to zero, so for g < -80 (rare) t is taken from
+// the accurate expf, which keeps silu(g) -- a normal fp32 number down to
+// about g = -92 -- instead of returning zero.
 __device__ __forceinline__ float silu_mul(float g, float u) {
-  return __fdividef(g, 1.0f + __expf(-g)) * u;
+  float t = __expf(-fabsf(g));
+  if (g < -80.f) t = expf(g);
+  return __fdividef(g >= 0.f ? g : g * t, 1.0f + t) * u;
 }
 
 // bf16x2 (S, S) for an e4m3 bit pattern, S = value * 2^116; NaN for S.1111.111.

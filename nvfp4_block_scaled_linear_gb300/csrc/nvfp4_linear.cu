@@ -30,9 +30,21 @@ constexpr double kGroupBytesPerStage = 16.0 * (256 / 2 + 256 / 16);
 constexpr double kWantInFlight = 128.0 * 1024;
 constexpr double kLoneCtaEfficiency = 0.74;
 constexpr int kTcgemmTilesPerCta = 4;
+// Wait limit under NVFP4_FLAG_TEST_STALL: long enough for the loads that are
+// issued, short enough for a test.
+constexpr uint64_t kTestStallWaitNs = 1000000ull;   // 1 ms
 
-// Bits set by kernels when a pipeline wait gives up (see ptx.cuh).
+// Bits set by kernels when a pipeline wait gives up (see ptx.cuh), and the
+// word as nvfp4_device_status last read it.
 __device__ unsigned int g_device_error;
+__device__ unsigned int g_device_error_read;
+
+// Read (and, if `clear`, reset) the error word in one atomic step, so that a
+// bit set by a kernel running meanwhile is either read or kept.
+__global__ void read_device_error_kernel(int clear) {
+  g_device_error_read =
+      clear ? atomicExch(&g_device_error, 0u) : atomicOr(&g_device_error, 0u);
+}
 
 constexpr int kMaxDevices = 64;
 constexpr int64_t kSmallMMax = 32;
@@ -71,7 +83,7 @@ struct DeviceInfo {
   int max_smem = 0;                    // opt-in shared memory per block
   int smem_per_sm = 0, smem_reserved = 0, regs_per_sm = 0, threads_per_sm = 0;
   unsigned int* err = nullptr;         // device address of g_device_error
-  int smallm_regs[3][5][sm::kMaxGroups + 1] = {};  // registers per thread by (CV, MT, G)
+  int smallm_regs[5][5][sm::kMaxGroups + 1] = {};  // registers per thread by (CV, MT, G)
   int gemv_regs[2] = {};               // registers per thread of the tcgen05 few-row kernel (N 16, 32)
   int gemv_bf16_regs[2][2] = {};       // the same, bf16 kernel, by (N 16 / 32, lane groups 2 / 4)
 };
@@ -178,6 +190,7 @@ int device_setup(DeviceInfo** out) {
           prepare_smallm<4, 0>(d) != cudaSuccess ||
           prepare_smallm<1, 1>(d) != cudaSuccess ||
           prepare_smallm<1, 2>(d) != cudaSuccess ||
+          prepare_smallm<1, 4>(d) != cudaSuccess ||
           prepare_gemv<16>(d) != cudaSuccess || prepare_gemv<32>(d) != cudaSuccess ||
           prepare_gemv_bf16<16, 2>(d) != cudaSuccess ||
           prepare_gemv_bf16<16, 4>(d) != cudaSuccess ||
@@ -288,7 +301,13 @@ int validate(const void* x, const void* wp, const void* ws, const void* y, int64
   if (!wp || !ws || (M > 0 && (!x || !y))) return NVFP4_ERR_INVALID;
   if (flags & ~(NVFP4_FLAG_SWIGLU | NVFP4_FLAG_F32_OUT | NVFP4_FLAG_FORCE_SMALLM |
                 NVFP4_FLAG_FORCE_TCGEMM | NVFP4_FLAG_SPLIT_MASK | NVFP4_FLAG_GROUPS_MASK |
-                NVFP4_FLAG_BF16_MMA | NVFP4_FLAG_FORCE_GEMV))
+                NVFP4_FLAG_BF16_MMA | NVFP4_FLAG_FORCE_GEMV | NVFP4_FLAG_TEST_STALL))
+    return NVFP4_ERR_INVALID;
+  // the wait-limit test hook: the warp-MMA kernel without a k split only
+  // (no cluster barrier and no TMEM for a stalled CTA to hold)
+  if ((flags & NVFP4_FLAG_TEST_STALL) &&
+      (!(flags & NVFP4_FLAG_FORCE_SMALLM) ||
+       (flags & NVFP4_FLAG_SPLIT_MASK) != NVFP4_FLAG_SPLIT(1)))
     return NVFP4_ERR_INVALID;
   if (((flags & NVFP4_FLAG_SPLIT_MASK) >> NVFP4_FLAG_SPLIT_SHIFT) > sm::kMaxSplit ||
       ((flags & NVFP4_FLAG_GROUPS_MASK) >> NVFP4_FLAG_GROUPS_SHIFT) > sm::kMaxGroups)
@@ -493,6 +512,8 @@ int launch_smallm(const DeviceInfo& d, const void* x, const uint8_t* wp, const u
   p.out_f32 = (flags & NVFP4_FLAG_F32_OUT) ? 1 : 0;
   p.swiglu = swiglu ? 1 : 0;
   p.err = d.err;
+  p.test_stall = (flags & NVFP4_FLAG_TEST_STALL) ? 1 : 0;
+  p.wait_ns = p.test_stall ? kTestStallWaitNs : nvfp4::kWaitTimeoutNs;
 
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof cfg);
@@ -826,14 +847,18 @@ int run(const void* x, const uint8_t* wp, const uint8_t* ws, float gs, float gs_
   if (kernel == NVFP4_KERNEL_SMALLM) {
     switch ((M + 7) / 8) {
       case 1:
-        // f16 with one activation converter up to M = 3, two from M = 4
-        // (verify, M = 7: 19.5 us against 22.4 with one; M = 5: 18.4
-        // against 19.6; decode, M = 1: 21.8 against 22.4 with two)
+        // f16 with one activation converter up to M = 3, two at M = 4 and
+        // four from M = 5: the converters' per-row work (the exponent and
+        // the f16 window check) sets the pace of a stage from M = 3 on
+        // (verify, M = 7: 21.3 us with four against 23.5 with two; decode,
+        // M = 1: 22.0 us with one)
         if (flags & NVFP4_FLAG_BF16_MMA)
           return launch_smallm<1, 0>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs, y_host);
         if (M <= 3)
           return launch_smallm<1, 1>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs, y_host);
-        return launch_smallm<1, 2>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs, y_host);
+        if (M == 4)
+          return launch_smallm<1, 2>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs, y_host);
+        return launch_smallm<1, 4>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs, y_host);
       case 2: return launch_smallm<2, 0>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs, y_host);
       case 3: return launch_smallm<3, 0>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs, y_host);
       default: return launch_smallm<4, 0>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs, y_host);
@@ -1130,16 +1155,18 @@ int nvfp4_device_status(unsigned int* bits, int clear) {
   DeviceInfo* d = nullptr;
   const int st = device_setup(&d);
   if (st != NVFP4_OK) return st;
-  if (cudaMemcpyFromSymbol(bits, g_device_error, sizeof(unsigned int)) != cudaSuccess) {
+  // Every stream of the device first (the copy below orders only against
+  // the legacy default stream, not against non-blocking streams), then the
+  // atomic read-and-clear, then its result.
+  if (cudaDeviceSynchronize() != cudaSuccess) {
     cudaGetLastError();
     return NVFP4_ERR_LAUNCH;
   }
-  if (clear) {
-    const unsigned int zero = 0;
-    if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero) != cudaSuccess) {
-      cudaGetLastError();
-      return NVFP4_ERR_LAUNCH;
-    }
+  read_device_error_kernel<<<1, 1, 0, 0>>>(clear ? 1 : 0);
+  if (cudaGetLastError() != cudaSuccess ||
+      cudaMemcpyFromSymbol(bits, g_device_error_read, sizeof(unsigned int)) != cudaSuccess) {
+    cudaGetLastError();
+    return NVFP4_ERR_LAUNCH;
   }
   return NVFP4_OK;
 }

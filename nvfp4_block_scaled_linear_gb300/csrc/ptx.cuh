@@ -60,11 +60,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait for the phase with the given parity to complete.  Gives up after
-// kWaitTimeoutNs and returns false; the caller records the failure and winds
-// down without waiting again.  `abort_flag` (shared memory) short-circuits
-// every later wait of the block once one wait has failed.
+// `timeout_ns` (kWaitTimeoutNs unless a kernel is told otherwise) and returns
+// false; the caller records the failure and winds down without waiting
+// again.  `abort_flag` (shared memory) short-circuits every later wait of the
+// block once one wait has failed.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
-                                          volatile int* abort_flag) {
+                                          volatile int* abort_flag,
+                                          uint64_t timeout_ns = kWaitTimeoutNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
@@ -74,7 +76,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
     for (int i = 0; i < 8; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (global_timer_ns() - t0 > kWaitTimeoutNs) {
+    if (global_timer_ns() - t0 > timeout_ns) {
       *abort_flag = 1;
       return false;
     }
@@ -223,8 +225,9 @@ __device__ __forceinline__ uint32_t f32x2_to_f16x2(float lo, float hi) {
   return d;
 }
 
-// Per-half unsigned max of two 16-bit pairs.
+// Per-half unsigned max and min of two 16-bit pairs.
 __device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) { return __vmaxu2(a, b); }
+__device__ __forceinline__ uint32_t min_u16x2(uint32_t a, uint32_t b) { return __vminu2(a, b); }
 
 // ---------------------------------------------------------------- tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {

@@ -29,7 +29,13 @@
 //    row, taken from that row's running maximum |x|.  Every activation within
 //    2^31 of its row's running maximum converts exactly, nothing overflows,
 //    and the fp32 accumulators are rescaled by exact powers of two when a
-//    row's maximum grows.
+//    row's maximum grows.  A row whose stage holds a nonzero value below that
+//    window is flagged by its converter: the consumers get zeros for it, and
+//    the converter itself multiplies that row's stage in bf16 (the bf16
+//    path's exact weights, the activations as given) into the CTA's partial
+//    sums, so the product is exact for every finite bf16 row while the
+//    consumers' loop, and every unflagged row, are exactly those of the plain
+//    f16 path.
 //  * Split-K: CTAs that share rows but not k form one thread-block cluster.
 //    Partials are reduced warp -> CTA in shared memory and then across the
 //    cluster through distributed shared memory.  No global workspace, no
@@ -134,6 +140,9 @@ struct Params {
   SmemLayout lay;
   SegScales seg;        // per-segment scales (seg.n == 0: out_scale for every column)
   unsigned int* err;    // device error word
+  uint64_t wait_ns;     // limit of every pipeline wait (kWaitTimeoutNs)
+  int test_stall;       // test hook: 1 = never load the last stage, so that the
+                        // waits for it run out (split 1 only)
 };
 
 // 2^a as fp32, a in [-126, 127].
@@ -149,8 +158,69 @@ __device__ __forceinline__ int next_slot(int slot, int stages, uint32_t& parity)
   return slot;
 }
 
-// CV: 0 for the bf16 path; 1 or 2 for the f16 path with that many
-// activation converter warps (two pay from M = 4 on, one is faster below).
+// The exact products of one stage for the flagged rows (bit m of `mine`) of
+// one converter warp, in bf16 on the warp MMA: the same fragment layout as
+// the consumers' bf16 path -- weights code * scale * 2^-10, activations as
+// given, paired (k, k+4) -- over all 16G rows and 256 k of the stage.  The
+// sums of the flagged rows' columns are added to the CTA's partials
+// [16G rows][8] (still carrying 2^-10; the consumers' reduction scales them
+// by 2^10); other columns stay zero and are not written.  Slow (about the
+// consumers' whole stage in one warp), taken only for rows outside the f16
+// window, and kept out of line so that it costs the converter's loop nothing
+// otherwise.
+template <int G>
+__device__ __noinline__ void flagged_rows_bf16(const uint8_t* st, uint32_t mine,
+                                               const SmemLayout& L, float* part, int lane) {
+  constexpr int C = 8;
+  const int g = lane >> 2, t = lane & 3;
+  const bool col_g = (mine >> g) & 1u;                  // B column g
+  const bool own0 = (mine >> (2 * t)) & 1u;             // D columns 2t, 2t + 1
+  const bool own1 = (mine >> (2 * t + 1)) & 1u;
+#pragma unroll 1
+  for (int r = 0; r < G; ++r) {
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+    for (int kq = 0; kq < kKQuarters; ++kq) {
+      uint4 c0 = make_uint4(0u, 0u, 0u, 0u), c1 = c0;
+      if (col_g) {
+        const uint8_t* xr = st + L.x_off + g * 512 + kq * 128 + t * 32;
+        c0 = *reinterpret_cast<const uint4*>(xr);
+        c1 = *reinterpret_cast<const uint4*>(xr + 16);
+      }
+      const uint32_t b[8] = {prmt(c0.x, c0.z, 0x5410u), prmt(c0.x, c0.z, 0x7632u),
+                             prmt(c0.y, c0.w, 0x5410u), prmt(c0.y, c0.w, 0x7632u),
+                             prmt(c1.x, c1.z, 0x5410u), prmt(c1.x, c1.z, 0x7632u),
+                             prmt(c1.y, c1.w, 0x5410u), prmt(c1.y, c1.w, 0x7632u)};
+      uint32_t pw[2][8];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int row = kGroupRows * r + 2 * g + h;
+        const int chunk = 2 * kq + (t >> 1);
+        const uint2 w = *reinterpret_cast<const uint2*>(
+            st + row * 128 + ((chunk ^ (row & 7)) << 4) + ((t & 1) << 3));
+        const uint32_t sc = scale_pair_from_e4m3(st[L.s_off + row * 16 + 4 * kq + t]);
+        dequant8_strided(w.x, sc, &pw[h][0]);
+        dequant8_strided(w.y, sc, &pw[h][4]);
+      }
+#pragma unroll
+      for (int s4 = 0; s4 < 4; ++s4)
+        mma_bf16_16816(d, pw[0][2 * s4], pw[1][2 * s4], pw[0][2 * s4 + 1], pw[1][2 * s4 + 1],
+                       b[2 * s4], b[2 * s4 + 1]);
+    }
+    const int ra = kGroupRows * r + 2 * g;
+    if (own0) {
+      part[ra * C + 2 * t] += d[0];
+      part[(ra + 1) * C + 2 * t] += d[2];
+    }
+    if (own1) {
+      part[ra * C + 2 * t + 1] += d[1];
+      part[(ra + 1) * C + 2 * t + 1] += d[3];
+    }
+  }
+}
+
+// CV: 0 for the bf16 path; 1, 2 or 4 for the f16 path with that many
+// activation converter warps (the host picks more as M grows).
 template <int MT, int G, int CV>
 __global__ void __launch_bounds__(threads_for(CV), CV > 0 ? 2 : 1)
     smallm_kernel(const __grid_constant__ CUtensorMap tm_w,
@@ -195,6 +265,10 @@ __global__ void __launch_bounds__(threads_for(CV), CV > 0 ? 2 : 1)
 
   for (int i = threadIdx.x; i < 256; i += kThreads)
     lut[i] = F16 ? scale_pair_f16_from_e4m3(i) : scale_pair_from_e4m3(i);
+  // f16 path: the converters add the bf16 products of flagged rows into the
+  // CTA's partials during the loop (the consumers' sums join them after it)
+  if (F16)
+    for (int i = threadIdx.x; i < rows * C; i += kThreads) part[i] = 0.f;
   if (threadIdx.x == 0) {
     for (int s = 0; s < L.stages; ++s) {
       mbar_init(&full[s], 1);
@@ -242,30 +316,38 @@ __global__ void __launch_bounds__(threads_for(CV), CV > 0 ? 2 : 1)
                              k0 + 64 * q, 0, pol_keep);
         }
       };
+      // Test hook: the last stage is never loaded, so every wait for it
+      // runs out (the host allows this only without a k split).
+      const int skipped = p.test_stall ? n_stages - 1 : -1;
       // The weights do not depend on the preceding kernel in the stream:
       // fill the ring with them first, then wait for that kernel before
       // touching the activations.
       const int pre = n_stages < L.stages ? n_stages : L.stages;
       for (int it = 0; it < pre; ++it) {
+        if (it == skipped) continue;
         mbar_arrive_expect_tx(&full[it], tx);
         issue_weights(it, it);
       }
       griddep_wait();
-      for (int it = 0; it < pre; ++it) issue_acts(it, it);
+      for (int it = 0; it < pre; ++it)
+        if (it != skipped) issue_acts(it, it);
       int issued = pre;
       int slot = pre == L.stages ? 0 : pre;
       uint32_t par = pre == L.stages ? 0u : 1u;
       for (int it = pre; it < n_stages; ++it) {
-        if (!mbar_wait(&empty[slot], par, abort_flag)) break;
-        mbar_arrive_expect_tx(&full[slot], tx);
-        issue_weights(it, slot);
-        issue_acts(it, slot);
+        if (!mbar_wait(&empty[slot], par, abort_flag, p.wait_ns)) break;
+        if (it != skipped) {
+          mbar_arrive_expect_tx(&full[slot], tx);
+          issue_weights(it, slot);
+          issue_acts(it, slot);
+        }
         ++issued;
         slot = next_slot(slot, L.stages, par);
       }
       // Drain: never leave a copy in flight into this CTA's shared memory.
       const int first = issued > L.stages ? issued - L.stages : 0;
       for (int it = first; it < issued; ++it) {
+        if (it == skipped) continue;
         volatile int no_abort = 0;
         if (!mbar_wait(&full[it % L.stages], (it / L.stages) & 1, &no_abort))
           atomicOr(p.err, kErrWaitTimeout);
@@ -280,7 +362,12 @@ __global__ void __launch_bounds__(threads_for(CV), CV > 0 ? 2 : 1)
     // chunk l (8 consecutive k) of each row of every stage.  a_run[i] is the
     // exponent of row c + CV * i: x is stored as f16(x * 2^a_run), with
     // a_run the largest value keeping the row's running maximum below 2^15
-    // (so no f16 overflow).
+    // (so no f16 overflow).  A bf16 value of biased exponent e converts to
+    // f16 exactly when e + a_run >= 110 (its last significant bit, at
+    // 2^(e - 134 + a_run), is then at or above f16's smallest step 2^-24).
+    // A row whose stage holds a nonzero value with a smaller exponent is
+    // flagged: it goes to the consumers as zeros, and this warp adds the
+    // row's exact bf16 products for the stage to the CTA's partials.
     constexpr int kConvWarps = CV > 0 ? CV : 1;
     constexpr int kRowsPer = kF16MaxRows / kConvWarps;
     const int c = warp - kConsumerWarps - 1;
@@ -303,30 +390,51 @@ __global__ void __launch_bounds__(threads_for(CV), CV > 0 ? 2 : 1)
           make_uint4(o[0], o[1], o[2], o[3]);
       if (lane == 0) reinterpret_cast<int*>(st + L.exp_off)[m] = a;
     };
+    // Warp-wide max |x| and (smallest nonzero |x|) - 1 of one row's 256 k, as
+    // bf16 magnitude bits.  Per 16-bit lane of a word of magnitudes,
+    // (h + 0x7FFF) & 0x7FFF is h - 1 for h > 0 and 0x7FFF for h = 0 (no carry
+    // crosses lanes: h <= 0x7FFF).
+    auto row_range = [&](const uint4& v, uint32_t& mx, uint32_t& mn) {
+      const uint32_t a0 = v.x & 0x7FFF7FFFu, a1 = v.y & 0x7FFF7FFFu;
+      const uint32_t a2 = v.z & 0x7FFF7FFFu, a3 = v.w & 0x7FFF7FFFu;
+      mx = max_u16x2(max_u16x2(a0, a1), max_u16x2(a2, a3));
+      mn = min_u16x2(min_u16x2((a0 + 0x7FFF7FFFu) & 0x7FFF7FFFu,
+                               (a1 + 0x7FFF7FFFu) & 0x7FFF7FFFu),
+                     min_u16x2((a2 + 0x7FFF7FFFu) & 0x7FFF7FFFu,
+                               (a3 + 0x7FFF7FFFu) & 0x7FFF7FFFu));
+      mx = __reduce_max_sync(0xffffffffu, max(mx & 0xFFFFu, mx >> 16));
+      mn = __reduce_min_sync(0xffffffffu, min(mn & 0xFFFFu, mn >> 16));
+    };
+    // flagged: a nonzero magnitude below (110 - a) << 7
+    auto out_of_window = [](uint32_t mn, int a) {
+      return static_cast<int>(mn) < (110 - a) * 128 - 1;
+    };
     int a_run[kRowsPer];
 #pragma unroll
     for (int i = 0; i < kRowsPer; ++i) a_run[i] = 126;
     int slot = 0;                 // ring position, stepped without a divide
     uint32_t par = 0;
     for (int it = 0; it < n_stages; ++it, slot = next_slot(slot, L.stages, par)) {
-      if (!mbar_wait(&full[slot], par, abort_flag)) break;
+      if (!mbar_wait(&full[slot], par, abort_flag, p.wait_ns)) break;
       uint8_t* st = smem + slot * L.stage_bytes;
+      uint32_t mine = 0;             // this converter's flagged rows (warp-uniform)
       if constexpr (CV == 1) {
         // one converter (M <= 3): row after row
 #pragma unroll
         for (int i = 0; i < kRowsPer; ++i) {
           if (i >= n_rows) break;
           const uint4 v = *reinterpret_cast<const uint4*>(st + L.x_off + i * 512 + lane * 16);
-          uint32_t mx = max_u16x2(max_u16x2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
-                                  max_u16x2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
-          mx = __reduce_max_sync(0xffffffffu, max(mx & 0xFFFFu, mx >> 16));
+          uint32_t mx, mn;
+          row_range(v, mx, mn);
           a_run[i] = min(a_run[i], max(-126, 141 - static_cast<int>(mx >> 7)));
+          mine |= out_of_window(mn, a_run[i]) ? 1u << i : 0u;
           convert_row(st, i, v, a_run[i]);
         }
       } else {
         // several converters (M >= 4): each converts all of its rows at once
         uint4 v[kRowsPer];
         int e_max[kRowsPer];
+        uint32_t mn[kRowsPer];
 #pragma unroll
         for (int i = 0; i < kRowsPer; ++i) {
           if (i >= n_rows) break;
@@ -336,27 +444,37 @@ __global__ void __launch_bounds__(threads_for(CV), CV > 0 ? 2 : 1)
 #pragma unroll
         for (int i = 0; i < kRowsPer; ++i) {
           if (i >= n_rows) break;
-          uint32_t mx = max_u16x2(max_u16x2(v[i].x & 0x7FFF7FFFu, v[i].y & 0x7FFF7FFFu),
-                                  max_u16x2(v[i].z & 0x7FFF7FFFu, v[i].w & 0x7FFF7FFFu));
-          mx = __reduce_max_sync(0xffffffffu, max(mx & 0xFFFFu, mx >> 16));
+          uint32_t mx;
+          row_range(v[i], mx, mn[i]);
           e_max[i] = static_cast<int>(mx >> 7);                // biased bf16 exponent
         }
 #pragma unroll
         for (int i = 0; i < kRowsPer; ++i) {
           if (i >= n_rows) break;
           a_run[i] = min(a_run[i], max(-126, 141 - e_max[i]));
+          mine |= out_of_window(mn[i], a_run[i]) ? 1u << (c + kConvWarps * i) : 0u;
           convert_row(st, c + kConvWarps * i, v[i], a_run[i]);
         }
       }
       // rows past M: a fixed exponent (their columns hold zeros)
       if (c == 0 && lane >= M && lane < kF16MaxRows)
         reinterpret_cast<int*>(st + L.exp_off)[lane] = 126;
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&conv[slot]);
-        mbar_arrive(&empty[slot]);
+      if (mine) {
+        // rare: the flagged rows go to the consumers as zeros (this lane's
+        // 16 bytes of each), and their exact products come from here
+        for (int m = 0; m < kF16MaxRows; ++m)
+          if ((mine >> m) & 1u)
+            *reinterpret_cast<uint4*>(st + L.x16_off + m * 512 + ((lane ^ (m & 7)) << 4)) =
+                make_uint4(0u, 0u, 0u, 0u);
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&conv[slot]);
+      if (mine) flagged_rows_bf16<G>(st, mine, L, part, lane);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[slot]);
     }
+    // the flagged rows' products are in the partials
+    asm volatile("bar.arrive 2, %0;" ::"n"((kConsumerWarps + CV) * 32) : "memory");
   } else if (warp < kConsumerWarps) {
     // ------------------------------------------------------------ consumers
     // warp = (k quarter kq, row-group parity rp): 64 k of every stage for
@@ -409,8 +527,8 @@ __global__ void __launch_bounds__(threads_for(CV), CV > 0 ? 2 : 1)
     int slot = 0;
     uint32_t par = 0;
     for (int it = 0; it < n_stages; ++it, slot = next_slot(slot, L.stages, par)) {
-      if (!mbar_wait(&full[slot], par, abort_flag)) break;
-      if (F16 && !mbar_wait(&conv[slot], par, abort_flag)) break;
+      if (!mbar_wait(&full[slot], par, abort_flag, p.wait_ns)) break;
+      if (F16 && !mbar_wait(&conv[slot], par, abort_flag, p.wait_ns)) break;
       const uint8_t* st = smem + slot * L.stage_bytes;
 
       uint32_t bx[MT][8];
@@ -508,8 +626,12 @@ __global__ void __launch_bounds__(threads_for(CV), CV > 0 ? 2 : 1)
     }
 
     // Warp partials -> ring (free now: every stage has been consumed once
-    // all consumer warps pass the barrier below).
-    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+    // all consumer warps -- and, on the f16 path, the converters, which read
+    // the ring for flagged rows -- pass the barrier below).
+    if (F16)
+      asm volatile("bar.sync 2, %0;" ::"n"((kConsumerWarps + CV) * 32) : "memory");
+    else
+      asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
     float* red = reinterpret_cast<float*>(smem);
 #pragma unroll
     for (int i = 0; i < RG; ++i) {
@@ -530,7 +652,8 @@ __global__ void __launch_bounds__(threads_for(CV), CV > 0 ? 2 : 1)
       float s = 0.f;
 #pragma unroll
       for (int q = 0; q < kKQuarters; ++q) s += red[q * rows * C + i];
-      part[i] = s;
+      // f16 path: plus the flagged rows' bf16 products (carrying 2^-10)
+      part[i] = F16 ? s + part[i] * kWeightPow2 : s;
     }
   }
 

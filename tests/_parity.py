@@ -3,10 +3,11 @@
 Tolerances (the accuracy contract of the layer):
   * fp32 results:  |y_gpu - y64| <= 1e-4 * A + 1e-6, where y64 is the oracle's
     fp64 result and A = sum_k |x w| (the oracle's companion output).
-  * bf16 results:  within 1 bf16 ulp of RNE_bf16(fp32(y64)), or -- near zero,
-    where the fp32 accumulation error allowed above can exceed one bf16 ulp --
-    within the fp32 tolerance plus half a bf16 ulp (the final rounding).
-    +0 and -0 are equal.
+  * bf16 results:  within 1 bf16 ulp of RNE_bf16(fp32(y64)); only near zero,
+    where the fp32 bound above exceeds one bf16 ulp of that rounded value, an
+    output may pass instead by lying within the fp32 bound plus half a bf16
+    ulp (the final rounding).  +0 and -0 are equal.  The count of outputs
+    that pass only that way (the strict-fail count) is returned.
   * SwiGLU (out = silu(g) * u): the accumulator errors propagate through
     d out = silu'(g) u dg + silu(g) du with |silu'| <= 1.1, plus a relative
     1e-5 for the fp32 exp/divide/multiply of the epilogue.
@@ -47,22 +48,46 @@ def check_f32(y_gpu, y64, a, what=""):
     return float(np.max(err / tol)) if err.size else 0.0
 
 
+def near_zero(ref_bits, a):
+    """Outputs whose fp32 error bound 1e-4*A+1e-6 exceeds one bf16 ulp of the
+    oracle's rounded value: there the fp32 accumulation the bound allows can
+    move the result by more than one bf16 ulp (cancellation, |y| << A)."""
+    return tol_f32(a) > bf16_ulp(bf16_bits_to_f64(ref_bits))
+
+
 def check_bf16(bits_gpu, y64, a, ref_bits, what=""):
-    """Returns (strict_fail_count, combined_fail_count); asserts combined == 0."""
+    """Returns (strict_fail_count, combined_fail_count); asserts combined == 0.
+
+    Strict: within 1 bf16 ulp of the oracle's RNE_bf16(fp32(y64)).  Only where
+    the output is near zero in the sense of near_zero() may an output outside
+    1 ulp pass instead by lying within the fp32 bound plus half a bf16 ulp (the
+    final rounding); everywhere else the 1-ulp rule alone applies.  NaN must
+    match NaN."""
     bits_gpu = np.asarray(bits_gpu, np.uint16)
     ulps = np.abs(_ordered(bits_gpu) - _ordered(ref_bits))
     strict_ok = ulps <= 1
     val = bf16_bits_to_f64(bits_gpu)
-    loose_ok = np.abs(val - y64) <= tol_f32(a) + 0.5 * bf16_ulp(val)
+    with np.errstate(invalid="ignore"):
+        loose_ok = near_zero(ref_bits, a) & (np.abs(val - y64) <= tol_f32(a) + 0.5 * bf16_ulp(val))
     ok = strict_ok | loose_ok
     nan_ref = np.isnan(y64)
     ok = np.where(nan_ref, np.isnan(val), ok)
     strict_fail = int((~strict_ok & ~nan_ref).sum())
     fail = int((~ok).sum())
-    assert fail == 0, "%s: %d/%d bf16 outputs outside 1 ulp and outside the fp32 tolerance; " \
-        "first at %s (gpu %s, oracle %s)" % (what, fail, ok.size, np.argwhere(~ok)[:3].tolist(),
-                                             val[~ok][:3], y64[~ok][:3])
+    assert fail == 0, "%s: %d/%d bf16 outputs outside 1 ulp (and, near zero, outside the fp32 " \
+        "tolerance); first at %s (gpu %s, oracle %s)" % (
+            what, fail, ok.size, np.argwhere(~ok)[:3].tolist(), val[~ok][:3], y64[~ok][:3])
     return strict_fail, fail
+
+
+def record(what, **counts):
+    """Append one JSON line of parity counts to $NVFP4_PARITY_LOG, if set."""
+    import json
+    import os
+    path = os.environ.get("NVFP4_PARITY_LOG")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps(dict(what=what, **counts)) + "\n")
 
 
 def swiglu_tol(y64_gate, y64_up, a_gate, a_up, out64):
@@ -82,12 +107,18 @@ def check_swiglu_f32(y_gpu, y64, a, out64, what=""):
 
 
 def check_swiglu_bf16(bits_gpu, y64, a, out64, ref_bits, what=""):
+    """As check_bf16 with the SwiGLU bound: the looser rule only where that
+    bound exceeds one bf16 ulp of the rounded oracle value.  Returns the
+    strict-fail count among outputs in fp32's normal range (|out| >= 2^-126;
+    below it fp32 itself holds fewer significant bits than bf16, and silu of
+    a very negative gate lands there)."""
     H = y64.shape[1] // 2
     tol = swiglu_tol(y64[:, :H], y64[:, H:], a[:, :H], a[:, H:], out64)
     bits_gpu = np.asarray(bits_gpu, np.uint16)
     ulps = np.abs(_ordered(bits_gpu) - _ordered(ref_bits))
     val = bf16_bits_to_f64(bits_gpu)
-    ok = (ulps <= 1) | (np.abs(val - out64) <= tol + 0.5 * bf16_ulp(val))
+    near = tol > bf16_ulp(bf16_bits_to_f64(ref_bits))
+    ok = (ulps <= 1) | (near & (np.abs(val - out64) <= tol + 0.5 * bf16_ulp(val)))
     assert ok.all(), "%s: %d/%d SwiGLU bf16 outputs outside tolerance; first at %s" % (
         what, (~ok).sum(), ok.size, np.argwhere(~ok)[:3].tolist())
-    return int((ulps > 1).sum())
+    return int(((ulps > 1) & (np.abs(out64) >= 2.0 ** -126)).sum())

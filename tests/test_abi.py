@@ -36,6 +36,7 @@ def test_header_constants_match_binding():
         assert "#define %s %du" % (name, value) in text or "#define %s %d " % (name, value) in text
     assert "#define NVFP4_FLAG_BF16_MMA (1u << 17)" in text and _lib.FLAG_BF16_MMA == 1 << 17
     assert "#define NVFP4_FLAG_FORCE_GEMV (1u << 18)" in text and _lib.FLAG_FORCE_GEMV == 1 << 18
+    assert "#define NVFP4_FLAG_TEST_STALL (1u << 19)" in text and _lib.FLAG_TEST_STALL == 1 << 19
     assert "#define NVFP4_FLAG_SPLIT_SHIFT 8" in text and _lib.FLAG_SPLIT(3) == 3 << 8
     assert "#define NVFP4_FLAG_GROUPS_SHIFT 13" in text and _lib.FLAG_GROUPS(5) == 5 << 13
 
@@ -81,6 +82,15 @@ def test_version_and_status_strings(lib):
     (-1, 256, 512, 0, _lib.KERNEL_NONE),
     (1, 256, 512, 64, _lib.KERNEL_NONE),                         # unknown flag
     (1, 256, 512, _lib.FLAG_FORCE_SMALLM | _lib.FLAG_FORCE_TCGEMM, _lib.KERNEL_NONE),
+    # the wait-limit test hook: warp-MMA kernel, split pinned to 1, only
+    (7, 256, 512, _lib.FLAG_FORCE_SMALLM | _lib.FLAG_SPLIT(1) | _lib.FLAG_TEST_STALL,
+     _lib.KERNEL_SMALLM),
+    (7, 256, 512, _lib.FLAG_TEST_STALL, _lib.KERNEL_NONE),
+    (7, 256, 512, _lib.FLAG_FORCE_SMALLM | _lib.FLAG_TEST_STALL, _lib.KERNEL_NONE),
+    (7, 256, 512, _lib.FLAG_FORCE_SMALLM | _lib.FLAG_SPLIT(2) | _lib.FLAG_TEST_STALL,
+     _lib.KERNEL_NONE),
+    (7, 256, 512, _lib.FLAG_FORCE_GEMV | _lib.FLAG_SPLIT(1) | _lib.FLAG_TEST_STALL,
+     _lib.KERNEL_NONE),
 ])
 def test_kernel_choice(lib, M, N, K, flags, expect):
     assert _lib.kernel_for(M, N, K, flags) == expect

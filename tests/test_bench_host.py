@@ -49,6 +49,10 @@ def test_reference_arm_prints_one_json_line():
     assert d["impl"] == "reference" and d["value"] > 0 and d["unit"] == "GB/s"
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0
+    # the same config object as the GPU arm prints for this workload
+    from nvfp4_block_scaled_linear_gb300.inputs import WORKLOADS
+    w = WORKLOADS["tiny"]
+    assert d["config"] == bench.workload_config("tiny", w.draw(), w.swiglu)
 
 
 def test_reference_arm_other_ranks_exit_silently():
