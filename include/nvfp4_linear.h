@@ -63,6 +63,7 @@ extern "C" {
 #define NVFP4_ERR_SHAPE (-3)        /* K % 256 != 0 or N % 128 != 0 */
 #define NVFP4_ERR_LAUNCH (-4)       /* the CUDA runtime refused the launch */
 #define NVFP4_ERR_DEVICE (-5)       /* no current device, or not an sm_103 GPU */
+#define NVFP4_ERR_TOO_LARGE (-6)    /* nvfp4_linear_host_noalloc: the call does not fit its scratch */
 
 /* Flags of nvfp4_linear_ex. */
 #define NVFP4_FLAG_SWIGLU 1u        /* fused gate/up: y = silu(gate) * up */
@@ -254,6 +255,47 @@ int nvfp4_linear_ex(const void* x, const uint8_t* w_packed, const uint8_t* w_sca
 int nvfp4_linear_host(const void* x_host, void* x_dev, const uint8_t* w_packed,
                       const uint8_t* w_scale, float global_scale, void* y_dev, void* y_host,
                       int64_t M, int64_t N, int64_t K, unsigned int flags, void* stream);
+
+/* Bytes of device scratch that nvfp4_linear_host_noalloc owns (8 MiB). */
+#define NVFP4_NOALLOC_SCRATCH_BYTES (8 * 1024 * 1024)
+
+/* nvfp4_linear_host for callers that cannot allocate device memory.  The
+ * pages have no counterpart: this is a convenience of this library.
+ *
+ * Some callers cannot call cudaMalloc -- a plug-in inside an application
+ * that owns every device allocation, a latency-bound loop where an
+ * allocation's implicit device synchronisation is not allowed, a process
+ * whose device memory is fully reserved -- yet hold the packed weights and
+ * scales on the device already and their activations in host memory.  This
+ * entry point runs the layer for them with no device buffer of theirs: the
+ * activations' device copy and the device result that nvfp4_linear_host
+ * stages through live in one array of NVFP4_NOALLOC_SCRATCH_BYTES that the
+ * library itself holds on every device that loads it, for the life of the
+ * process.  It allocates nothing: no cudaMalloc, no cudaFree, no allocating
+ * library routine.
+ *   x_host, y_host, w_packed, w_scale, global_scale, M, N, K, flags, stream:
+ *           as for nvfp4_linear_host (x_host bf16 [M, K] in host memory;
+ *           y_host the result in host memory, [M, N] or [M, N/2] with
+ *           SWIGLU, bf16 or fp32 with F32_OUT).  Page-locked host buffers
+ *           go zero-copy, others through cudaMemcpyAsync (pageable memory
+ *           then makes the copies synchronise with the host).
+ * Limit: the activations (M * K * 2 bytes, rounded up to 256) and the
+ * result (M * N_out * 2 or 4 bytes) must fit in NVFP4_NOALLOC_SCRATCH_BYTES
+ * together; otherwise NVFP4_ERR_TOO_LARGE and nothing is launched.  (Decode,
+ * verify and the M = 32 layer's linears of a 5120-wide model fit; a prefill
+ * chunk does not.)  Other errors as nvfp4_linear_host.
+ * Set-up: the first call on a device looks up the array's device address
+ * with that device current; make that first call before any stream capture.
+ * Sharing: every call on a device uses the same array, which keeps the last
+ * call's contents.  Nothing in it has to start at zero: each call writes
+ * the activations' part and the result's part before reading them.  Calls
+ * whose work can overlap on the GPU -- calls on different streams, or from
+ * host threads that do not order them on one stream -- race on the array;
+ * calls enqueued one after another on one stream do not. */
+int nvfp4_linear_host_noalloc(const void* x_host, const uint8_t* w_packed,
+                              const uint8_t* w_scale, float global_scale, void* y_host,
+                              int64_t M, int64_t N, int64_t K, unsigned int flags,
+                              void* stream);
 
 /* Which kernel a call with these sizes and flags would launch
  * (NVFP4_KERNEL_*), or NVFP4_KERNEL_NONE if the call would be rejected.

@@ -35,6 +35,9 @@ def FLAG_GROUPS(n):
     return (int(n) & 0xF) << 13
 
 
+ERR_TOO_LARGE = -6                # nvfp4_linear_host_noalloc: beyond its scratch
+NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
+
 KERNEL_NONE, KERNEL_SMALLM, KERNEL_TCGEMM, KERNEL_GEMV, KERNEL_GEMV_BF16 = 0, 1, 2, 3, 4
 KERNEL_NAMES = {KERNEL_SMALLM: "smallm", KERNEL_TCGEMM: "tcgemm", KERNEL_GEMV: "gemv_tc",
                 KERNEL_GEMV_BF16: "gemv_bf16"}
@@ -84,6 +87,8 @@ def load_library(path=None):
     lib.nvfp4_linear_ex.argtypes = [P, P, P, ctypes.c_float, P, i64, i64, i64, u32, P]
     lib.nvfp4_linear_host.restype = ctypes.c_int
     lib.nvfp4_linear_host.argtypes = [P, P, P, P, ctypes.c_float, P, P, i64, i64, i64, u32, P]
+    lib.nvfp4_linear_host_noalloc.restype = ctypes.c_int
+    lib.nvfp4_linear_host_noalloc.argtypes = [P, P, P, ctypes.c_float, P, i64, i64, i64, u32, P]
     lib.nvfp4_linear_swiglu_gs.restype = ctypes.c_int
     lib.nvfp4_linear_swiglu_gs.argtypes = [P, P, P, ctypes.c_float, ctypes.c_float, P, i64, i64,
                                            i64, u32, P]
@@ -214,6 +219,38 @@ def linear_host(x_host, x_dev, w_packed, w_scale, global_scale, y_dev, y_host, f
                                          ctypes.c_void_p(stream.cuda_stream))
     if st != OK:
         raise Nvfp4Error(st, "nvfp4_linear_host")
+    return y_host
+
+
+def linear_host_noalloc(x_host, w_packed, w_scale, global_scale, y_host, flags=0, stream=None):
+    """Call nvfp4_linear_host_noalloc: the layer on host activations
+    ``x_host`` into the host tensor ``y_host``, staged through the library's
+    own fixed device scratch (no device buffer from the caller).  Returns
+    ``y_host``."""
+    if not (w_packed.is_cuda and w_scale.is_cuda):
+        raise ValueError("w_packed and w_scale must be CUDA tensors")
+    w_packed, w_scale = _as_u8(w_packed, "w_packed"), _as_u8(w_scale, "w_scale")
+    if x_host.is_cuda or y_host.is_cuda:
+        raise ValueError("x_host and y_host must be in host memory")
+    if x_host.dtype != torch.bfloat16 or x_host.dim() != 2 or not x_host.is_contiguous():
+        raise TypeError("x_host must be a contiguous 2-D bfloat16 tensor")
+    M, K = x_host.shape
+    N = w_packed.shape[0]
+    if tuple(w_packed.shape) != (N, K // 2) or tuple(w_scale.shape) != (N, K // 16):
+        raise ValueError("shapes disagree: x %s, w_packed %s, w_scale %s"
+                         % (tuple(x_host.shape), tuple(w_packed.shape), tuple(w_scale.shape)))
+    n_out = N // 2 if flags & FLAG_SWIGLU else N
+    dtype = torch.float32 if flags & FLAG_F32_OUT else torch.bfloat16
+    if y_host.dtype != dtype or tuple(y_host.shape) != (M, n_out) or not y_host.is_contiguous():
+        raise ValueError("y_host must be a contiguous %s tensor of shape %s" % (dtype, (M, n_out)))
+    if stream is None:
+        stream = torch.cuda.current_stream(w_packed.device)
+    with _on_device(w_packed.device):
+        st = library().nvfp4_linear_host_noalloc(
+            x_host.data_ptr(), w_packed.data_ptr(), w_scale.data_ptr(), float(global_scale),
+            y_host.data_ptr(), M, N, K, int(flags), ctypes.c_void_p(stream.cuda_stream))
+    if st != OK:
+        raise Nvfp4Error(st, "nvfp4_linear_host_noalloc")
     return y_host
 
 

@@ -934,6 +934,8 @@ const char* nvfp4_status_string(int status) {
     case NVFP4_ERR_SHAPE: return "unsupported shape (need K % 256 == 0 and N % 128 == 0)";
     case NVFP4_ERR_LAUNCH: return "CUDA launch failed";
     case NVFP4_ERR_DEVICE: return "no usable sm_103 device";
+    case NVFP4_ERR_TOO_LARGE:
+      return "activations plus result exceed the fixed scratch of nvfp4_linear_host_noalloc";
     default: return "unknown status";
   }
 }
@@ -1148,6 +1150,75 @@ int nvfp4_linear_kernel_for(int64_t M, int64_t N, int64_t K, unsigned int flags)
   if (validate(dummy, dummy, dummy, dummy, M, N, K, flags) != NVFP4_OK || M == 0)
     return NVFP4_KERNEL_NONE;
   return kernel_for(M, N, K, flags);
+}
+
+}  // extern "C"
+
+// ------------------------------------------------------------------------
+// nvfp4_linear_host_noalloc: nvfp4_linear_host with its two device staging
+// buffers (the activations' copy on the device and the result before it
+// goes back to the host) carved from one fixed array of this library, so
+// that the caller allocates no device memory at all.  The array is a
+// file-scope __device__ object: every device that loads the library holds
+// it for the life of the process.  Its name, in host code, is only a host
+// stand-in for the symbol, so its device address is looked up once per
+// device (cudaGetSymbolAddress, that device current) and cached.
+namespace {
+
+__device__ __align__(256) unsigned char g_host_scratch[NVFP4_NOALLOC_SCRATCH_BYTES];
+
+std::mutex g_scratch_mutex;
+void* g_scratch_addr[kMaxDevices] = {};
+
+// Device address of g_host_scratch on the current device (set up on the
+// first call there); nullptr and a status on failure.
+void* host_scratch(int* status) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    *status = NVFP4_ERR_DEVICE;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (!g_scratch_addr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_host_scratch) != cudaSuccess || !ptr) {
+      cudaGetLastError();
+      *status = NVFP4_ERR_DEVICE;
+      return nullptr;
+    }
+    g_scratch_addr[dev] = ptr;
+  }
+  *status = NVFP4_OK;
+  return g_scratch_addr[dev];
+}
+
+}  // namespace
+
+extern "C" {
+
+int nvfp4_linear_host_noalloc(const void* x_host, const uint8_t* w_packed,
+                              const uint8_t* w_scale, float global_scale, void* y_host,
+                              int64_t M, int64_t N, int64_t K, unsigned int flags,
+                              void* stream) {
+  if (M < 0 || N <= 0 || K <= 0) return NVFP4_ERR_INVALID;
+  if (M == 0) return NVFP4_OK;
+  if (!x_host || !y_host) return NVFP4_ERR_INVALID;
+  // sizes first, with no overflow: M, N, K are bounded before they multiply
+  if (M > (int64_t(1) << 24) || N > (int64_t(1) << 31) || K > (int64_t(1) << 31))
+    return NVFP4_ERR_TOO_LARGE;
+  const int64_t n_out = (flags & NVFP4_FLAG_SWIGLU) ? N / 2 : N;
+  const int64_t x_bytes = M * K * 2;
+  const int64_t x_span = (x_bytes + 255) / 256 * 256;       // y starts 256-aligned
+  const int64_t y_bytes = M * n_out * ((flags & NVFP4_FLAG_F32_OUT) ? 4 : 2);
+  if (x_bytes > NVFP4_NOALLOC_SCRATCH_BYTES ||
+      y_bytes > NVFP4_NOALLOC_SCRATCH_BYTES - x_span)
+    return NVFP4_ERR_TOO_LARGE;
+  int st = NVFP4_OK;
+  unsigned char* scratch = static_cast<unsigned char*>(host_scratch(&st));
+  if (!scratch) return st;
+  return nvfp4_linear_host(x_host, scratch, w_packed, w_scale, global_scale, scratch + x_span,
+                           y_host, M, N, K, flags, stream);
 }
 
 int nvfp4_device_status(unsigned int* bits, int clear) {

@@ -43,7 +43,7 @@ def test_header_constants_match_binding():
 
 def test_version_and_status_strings(lib):
     assert _lib.abi_version() == 1
-    for st in (0, -1, -2, -3, -4, -5, 7):
+    for st in (0, -1, -2, -3, -4, -5, -6, 7):
         s = _lib.status_string(st)
         assert isinstance(s, str) and s
 
@@ -165,6 +165,13 @@ def test_rejects_before_any_device_work(lib):
     assert h(H, A, A, A, ctypes.c_float(1.0), A + 2, H, 1, 256, 512, 0, None) == -2
     assert h(H, A, A, A, ctypes.c_float(1.0), A, H, 1, 256, 384, 0, None) == -3
     assert h(None, None, A, A, ctypes.c_float(1.0), None, None, 0, 256, 512, 0, None) == 0
+    na = lib.nvfp4_linear_host_noalloc
+    assert na(None, A, A, ctypes.c_float(1.0), H, 1, 256, 512, 0, None) == -1
+    assert na(H, A, A, ctypes.c_float(1.0), None, 1, 256, 512, 0, None) == -1
+    assert na(H, A, A, ctypes.c_float(1.0), H, -1, 256, 512, 0, None) == -1
+    assert na(None, A, A, ctypes.c_float(1.0), None, 0, 256, 512, 0, None) == 0
+    assert na(H, A, A, ctypes.c_float(1.0), H, 8192, 34816, 5120, 0, None) == -6   # too large
+    assert _lib.status_string(-6) != _lib.status_string(99)
     # tuning overrides out of range
     assert lib.nvfp4_linear_ex(A, A, A, ctypes.c_float(1.0), A, 1, 256, 512,
                                _lib.FLAG_SPLIT(17), None) == -1
