@@ -29,7 +29,10 @@ namespace gb = nvfp4::gemvbf;
 constexpr double kGroupBytesPerStage = 16.0 * (256 / 2 + 256 / 16);
 constexpr double kWantInFlight = 128.0 * 1024;
 constexpr double kLoneCtaEfficiency = 0.74;
-constexpr int kTcgemmTilesPerCta = 4;
+// Activation tiles per band of the tensor-core kernel's tile order (16
+// tiles of 256 rows of a 5120-wide x: 42 MB, kept in L2 while the band's
+// weights stream past).
+constexpr int kTcgemmBand = 16;
 // Wait limit under NVFP4_FLAG_TEST_STALL: long enough for the loads that are
 // issued, short enough for a test.
 constexpr uint64_t kTestStallWaitNs = 1000000ull;   // 1 ms
@@ -801,11 +804,13 @@ int launch_tcgemm(const DeviceInfo& d, const void* x, const uint8_t* wp, const u
   const int64_t tiles_x = (M + T::kTileX - 1) / T::kTileX;
   if (tiles_w * tiles_x > INT32_MAX) return NVFP4_ERR_SHAPE;
   p.tiles_w = static_cast<int>(tiles_w);
+  p.tiles_x = static_cast<int>(tiles_x);
   p.tiles_total = static_cast<int>(tiles_w * tiles_x);
-  p.tiles_per_cta = kTcgemmTilesPerCta;
+  p.band = static_cast<int>(std::min<int64_t>(tiles_x, kTcgemmBand));
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof cfg);
-  cfg.gridDim = dim3(static_cast<unsigned>((p.tiles_total + p.tiles_per_cta - 1) / p.tiles_per_cta), 1, 1);
+  // persistent: one CTA per SM (its shared memory and TMEM allow no more)
+  cfg.gridDim = dim3(static_cast<unsigned>(std::min<int64_t>(p.tiles_total, d.num_sms)), 1, 1);
   cfg.blockDim = dim3(T::kThreads, 1, 1);
   cfg.dynamicSmemBytes = T::kSmemBytes;
   cfg.stream = stream;

@@ -4,6 +4,7 @@
 #pragma once
 #include <cstdint>
 #include <cuda.h>
+#include <cuda_bf16.h>
 
 namespace nvfp4 {
 
@@ -125,6 +126,28 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
 // tensor core).
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Stores marked as streaming (cache-streaming, likely accessed once): they
+// are the first candidates for eviction from L2.
+__device__ __forceinline__ void st_global_cs(float* p, float v) {
+  asm volatile("st.global.cs.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
+}
+__device__ __forceinline__ void st_global_cs(__nv_bfloat16* p, __nv_bfloat16 v) {
+  asm volatile("st.global.cs.b16 [%0], %1;" ::"l"(p), "h"(__bfloat16_as_ushort(v)) : "memory");
+}
+__device__ __forceinline__ void st_global_cs(uint32_t* p, uint32_t v) {
+  asm volatile("st.global.cs.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_global_cs(float2* p, float2 v) {
+  asm volatile("st.global.cs.v2.f32 [%0], {%1, %2};" ::"l"(p), "f"(v.x), "f"(v.y) : "memory");
+}
+
+// Two fp32 -> bf16x2 (lo in the low half), round to nearest even.
+__device__ __forceinline__ uint32_t f32x2_to_bf16x2(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
 }
 
 // ---------------------------------------------------------------- PDL

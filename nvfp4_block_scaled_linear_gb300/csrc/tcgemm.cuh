@@ -10,10 +10,15 @@
 // the other orientation.  D = W x^T sits in TMEM as 128 lanes (weight rows)
 // x 256 f32 columns (activation rows).
 //
-// Persistent: one CTA per SM walks the output tiles (activation tiles
-// outermost, so that a wave of CTAs shares one activation tile in L2), and
-// the accumulator is double-buffered in TMEM (2 x 256 columns) so that the
-// epilogue of one tile overlaps the k loop of the next.
+// Persistent: one CTA per SM, each walking the output tiles with the grid as
+// its stride, and the accumulator double-buffered in TMEM (2 x 256 columns)
+// so that the epilogue of one tile overlaps the k loop of the next.  Tile
+// order: bands of `band` activation tiles (42 MB of a 5120-wide x for 16
+// tiles), within a band weight tile by weight tile, the band's activation
+// tiles innermost.  The CTAs working at one time then take a few weight
+// tiles, each shared by `band` of them, and the whole band's activations,
+// which the copies mark evict-last so that they stay in L2 while the band's
+// weights stream past once; the results are stored as streaming data.
 //
 // Warp roles (448 threads):
 //   warp 0      TMA producer: activation tile (128B-swizzled, the B operand
@@ -71,8 +76,9 @@ struct Params {
   int out_f32;
   int swiglu;          // tile = 64 gate rows + the 64 matching up rows
   int tiles_w;         // weight tiles (N / 128)
+  int tiles_x;         // activation tiles (M / 256, rounded up)
   int tiles_total;     // weight tiles x activation tiles
-  int tiles_per_cta;   // consecutive tiles each CTA takes
+  int band;            // activation tiles per band of the tile order
   SegScales seg;        // per-segment scales (seg.n == 0: out_scale for every column)
   unsigned int* err;
 };
@@ -96,14 +102,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_stages = static_cast<int>(p.K / kStageK);
-  // This CTA's tiles: t = blockIdx.x * tiles_per_cta + i, i < my_tiles;
-  // tile t = (weight tile t % tiles_w, activation tile t / tiles_w).
-  const int t0 = blockIdx.x * p.tiles_per_cta;
-  const int my_tiles = min(p.tiles_per_cta, p.tiles_total - t0);
+  // This CTA's tiles: t = blockIdx.x + i * gridDim.x, i < my_tiles.  Tile t
+  // lies in band t / (tiles_w * band); within the band, weight tile by
+  // weight tile, activation tiles innermost (the last band may be narrower).
+  const int grid = static_cast<int>(gridDim.x);
+  const int my_tiles = static_cast<int>(blockIdx.x) < p.tiles_total
+                           ? (p.tiles_total - 1 - static_cast<int>(blockIdx.x)) / grid + 1
+                           : 0;
   auto tile_of = [&](int i, int& bw, int& m_tile) {
-    const int t = t0 + i;
-    bw = t % p.tiles_w;
-    m_tile = (t / p.tiles_w) * kTileX;
+    const int t = static_cast<int>(blockIdx.x) + i * grid;
+    const int per_band = p.tiles_w * p.band;
+    const int band = t / per_band;
+    const int r = t - band * per_band;
+    const int a0 = band * p.band;
+    const int width = min(p.band, p.tiles_x - a0);
+    bw = r / width;
+    m_tile = (a0 + (r - bw * width)) * kTileX;
   };
   // weight rows feeding A rows [0,64) and [64,128) of weight tile bw
   auto wrows = [&](int bw, int& wrow0, int& wrow1) {
@@ -149,7 +163,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tensormap(&tm_x);
       prefetch_tensormap(&tm_w);
       prefetch_tensormap(&tm_s);
-      const uint64_t pol_w = policy_evict_last();    // weights: reused by M tiles
+      // activations: reused by every weight tile of their band; weights:
+      // read by the band's CTAs at about the same time, then not again
+      const uint64_t pol_x = policy_evict_last();
       // Cursor over (tile i, stage it): the single producer thread must not
       // spend its stage budget on divisions, so tile coordinates change only
       // at tile boundaries.
@@ -170,17 +186,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto issue_weights = [&](const Cursor& c, int slot) {
         uint8_t* st = smem + slot * kStageBytes;
         const int k0 = c.it * kStageK;
-        tma_load_2d_hint(st + kRawOff, &tm_w, &tma_full[slot], k0 / 2, c.wrow0, pol_w);
-        tma_load_2d_hint(st + kRawOff + kRawBytes / 2, &tm_w, &tma_full[slot], k0 / 2, c.wrow1,
-                         pol_w);
+        tma_load_2d(st + kRawOff, &tm_w, &tma_full[slot], k0 / 2, c.wrow0);
+        tma_load_2d(st + kRawOff + kRawBytes / 2, &tm_w, &tma_full[slot], k0 / 2, c.wrow1);
         const int sx = (k0 / 16) & ~15;
-        tma_load_2d_hint(st + kSclOff, &tm_s, &tma_full[slot], sx, c.wrow0, pol_w);
-        tma_load_2d_hint(st + kSclOff + kSclBytes / 2, &tm_s, &tma_full[slot], sx, c.wrow1,
-                         pol_w);
+        tma_load_2d(st + kSclOff, &tm_s, &tma_full[slot], sx, c.wrow0);
+        tma_load_2d(st + kSclOff + kSclBytes / 2, &tm_s, &tma_full[slot], sx, c.wrow1);
       };
       auto issue_acts = [&](const Cursor& c, int slot) {
-        tma_load_2d(smem + slot * kStageBytes + kXOff, &tm_x, &tma_full[slot], c.it * kStageK,
-                    c.m_tile);
+        tma_load_2d_hint(smem + slot * kStageBytes + kXOff, &tm_x, &tma_full[slot],
+                         c.it * kStageK, c.m_tile, pol_x);
       };
       Cursor cur{0, 0, 0, 0, 0};
       if (my_tiles > 0) start_tile(cur);
@@ -328,23 +342,57 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&acc_empty[b]);
         }
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int m = m_tile + c0 + j;
-          float yv = __uint_as_float(v[j]) * lane_scale;
-          if (p.swiglu) {
-            // lanes 2k (gate) and 2k+1 (up) share output column ncol; the
-            // even lane takes the even activation rows, the odd lane the odd
-            const float other = __shfl_xor_sync(0xffffffffu, yv, 1);
-            if ((j & 1) != (lane & 1)) continue;
-            yv = (lane & 1) ? silu_mul(other, yv) : silu_mul(yv, other);
-          }
-          if (m >= p.M) continue;
+        // Written once, read by the next layer: streaming stores, so that
+        // the results do not push the band's activations out of L2.
+        auto store = [&](int m, float yv) {
+          if (m >= p.M) return;
           const int64_t off = static_cast<int64_t>(m) * n_out + ncol;
           if (p.out_f32)
-            static_cast<float*>(p.y)[off] = yv;
+            st_global_cs(static_cast<float*>(p.y) + off, yv);
           else
-            static_cast<__nv_bfloat16*>(p.y)[off] = __float2bfloat16_rn(yv);
+            st_global_cs(static_cast<__nv_bfloat16*>(p.y) + off, __float2bfloat16_rn(yv));
+        };
+        if (p.swiglu) {
+          // Lanes 2k (gate) and 2k+1 (up) share output column ncol; the
+          // even lane produces the even activation rows of the chunk, the
+          // odd lane the odd ones.  Per pair of rows each lane sends the
+          // value of the row its partner produces and receives the other
+          // half of its own row's pair: one exchange per two rows, every
+          // lane busy (no divergent half-warp).
+          const int odd = lane & 1;
+          const float s_gate = p.seg.n ? lane_scale : p.out_scale;
+          const float s_up = p.seg.n ? lane_scale : p.out_scale_up;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float mine = __uint_as_float(odd ? v[2 * i + 1] : v[2 * i]);
+            const float send = __uint_as_float(odd ? v[2 * i] : v[2 * i + 1]);
+            const float recv = __shfl_xor_sync(0xffffffffu, send, 1);
+            const float g = (odd ? recv : mine) * s_gate;
+            const float u = (odd ? mine : recv) * s_up;
+            store(m_tile + c0 + 2 * i + odd, silu_mul(g, u));
+          }
+        } else {
+          // Lanes 2k and 2k+1 hold adjacent output columns: per pair of
+          // rows each lane sends its partner one value and stores both
+          // columns of one row as a single 4-byte (f32: 8-byte) word.
+          const int odd = lane & 1;
+          const int64_t col0 = ncol - odd;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float a0 = __uint_as_float(v[2 * i]) * lane_scale;
+            const float a1 = __uint_as_float(v[2 * i + 1]) * lane_scale;
+            const float recv = __shfl_xor_sync(0xffffffffu, odd ? a0 : a1, 1);
+            const int m = m_tile + c0 + 2 * i + odd;
+            if (m >= p.M) continue;
+            const float lo = odd ? recv : a0, hi = odd ? a1 : recv;
+            const int64_t off = static_cast<int64_t>(m) * n_out + col0;
+            if (p.out_f32)
+              st_global_cs(reinterpret_cast<float2*>(static_cast<float*>(p.y) + off),
+                           make_float2(lo, hi));
+            else
+              st_global_cs(reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(p.y) + off),
+                           f32x2_to_bf16x2(lo, hi));
+          }
         }
       }
     }
