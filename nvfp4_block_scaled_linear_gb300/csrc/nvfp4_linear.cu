@@ -54,27 +54,28 @@ constexpr int64_t kSmallMMax = 32;
 
 using SmallmFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, sm::Params);
 
-// The few-row kernel instance for (MT, G, CV) (CV: 0 bf16, 1 or 2 f16 with
-// that many activation converters); combinations the kernel does not
-// support are never instantiated.
-template <int MT, int G, int CV>
+// The few-row kernel instance for (MT, G, CV, W) (CV: 0 bf16, 1, 2 or 4 f16
+// with that many activation converters; W: consumer row-group ways, 4 only
+// for bf16); combinations the kernel does not support are never
+// instantiated.
+template <int MT, int G, int CV, int W>
 constexpr SmallmFn smallm_instance() {
-  if constexpr (G <= sm::max_groups(MT) && (CV == 0 || MT == 1))
-    return &sm::smallm_kernel<MT, G, CV>;
+  if constexpr (G <= sm::max_groups(MT) && (CV == 0 || MT == 1) && (W == sm::kWays || CV == 0))
+    return &sm::smallm_kernel<MT, G, CV, W>;
   else
     return nullptr;
 }
-template <int MT, int CV>
+template <int MT, int CV, int W = sm::kWays>
 SmallmFn smallm_fn(int g) {
   switch (g) {
-    case 1: return smallm_instance<MT, 1, CV>();
-    case 2: return smallm_instance<MT, 2, CV>();
-    case 3: return smallm_instance<MT, 3, CV>();
-    case 4: return smallm_instance<MT, 4, CV>();
-    case 5: return smallm_instance<MT, 5, CV>();
-    case 6: return smallm_instance<MT, 6, CV>();
-    case 7: return smallm_instance<MT, 7, CV>();
-    case 8: return smallm_instance<MT, 8, CV>();
+    case 1: return smallm_instance<MT, 1, CV, W>();
+    case 2: return smallm_instance<MT, 2, CV, W>();
+    case 3: return smallm_instance<MT, 3, CV, W>();
+    case 4: return smallm_instance<MT, 4, CV, W>();
+    case 5: return smallm_instance<MT, 5, CV, W>();
+    case 6: return smallm_instance<MT, 6, CV, W>();
+    case 7: return smallm_instance<MT, 7, CV, W>();
+    case 8: return smallm_instance<MT, 8, CV, W>();
     default: return nullptr;
   }
 }
@@ -86,7 +87,8 @@ struct DeviceInfo {
   int max_smem = 0;                    // opt-in shared memory per block
   int smem_per_sm = 0, smem_reserved = 0, regs_per_sm = 0, threads_per_sm = 0;
   unsigned int* err = nullptr;         // device address of g_device_error
-  int smallm_regs[5][5][sm::kMaxGroups + 1] = {};  // registers per thread by (CV, MT, G)
+  // registers per thread of the warp-MMA kernel by (W == 4, CV, MT, G)
+  int smallm_regs[2][5][5][sm::kMaxGroups + 1] = {};
   int gemv_regs[2] = {};               // registers per thread of the tcgen05 few-row kernel (N 16, 32)
   int gemv_bf16_regs[2][2] = {};       // the same, bf16 kernel, by (N 16 / 32, lane groups 2 / 4)
 };
@@ -95,10 +97,10 @@ std::mutex g_mutex;
 DeviceInfo g_dev[kMaxDevices];
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
-template <int MT, int CV>
+template <int MT, int CV, int W = sm::kWays>
 cudaError_t prepare_smallm(DeviceInfo& d) {
   for (int g = 1; g <= sm::max_groups(MT); ++g) {
-    const SmallmFn kern = smallm_fn<MT, CV>(g);
+    const SmallmFn kern = smallm_fn<MT, CV, W>(g);
     if (!kern) continue;
     cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, d.max_smem);
@@ -107,7 +109,7 @@ cudaError_t prepare_smallm(DeviceInfo& d) {
     cudaFuncAttributes fa;
     if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, kern);
     if (e != cudaSuccess) return e;
-    d.smallm_regs[CV][MT][g] = fa.numRegs;
+    d.smallm_regs[W == 4][CV][MT][g] = fa.numRegs;
   }
   return cudaSuccess;
 }
@@ -188,12 +190,12 @@ int device_setup(DeviceInfo** out) {
       void* err_addr = nullptr;
       if (cudaGetSymbolAddress(&err_addr, g_device_error) != cudaSuccess ||
           prepare_smallm<1, 0>(d) != cudaSuccess ||
-          prepare_smallm<2, 0>(d) != cudaSuccess ||
           prepare_smallm<3, 0>(d) != cudaSuccess ||
           prepare_smallm<4, 0>(d) != cudaSuccess ||
           prepare_smallm<1, 1>(d) != cudaSuccess ||
           prepare_smallm<1, 2>(d) != cudaSuccess ||
           prepare_smallm<1, 4>(d) != cudaSuccess ||
+          prepare_smallm<2, 0, 4>(d) != cudaSuccess ||
           prepare_gemv<16>(d) != cudaSuccess || prepare_gemv<32>(d) != cudaSuccess ||
           prepare_gemv_bf16<16, 2>(d) != cudaSuccess ||
           prepare_gemv_bf16<16, 4>(d) != cudaSuccess ||
@@ -415,7 +417,7 @@ struct SmallmPlan {
 // the rings of an SM hold less than ~128 KB of weights in flight; grids that
 // are resident in one wave win over those that are not; ties go to fewer
 // CTAs.  Overrides in `flags` pin G or the split.
-template <int MT, int CV>
+template <int MT, int CV, int W>
 SmallmPlan plan_smallm(const DeviceInfo& d, int64_t M, int64_t N, int64_t K,
                        unsigned int flags) {
   const bool swiglu = flags & NVFP4_FLAG_SWIGLU;
@@ -424,7 +426,7 @@ SmallmPlan plan_smallm(const DeviceInfo& d, int64_t M, int64_t N, int64_t K,
   const int want_groups = (flags & NVFP4_FLAG_GROUPS_MASK) >> NVFP4_FLAG_GROUPS_SHIFT;
   const int64_t unit_rows = swiglu ? N / 2 : N;
   constexpr bool F16 = CV > 0;
-  const int threads = sm::threads_for(CV);
+  const int threads = sm::threads_for(CV, W);
   static const int kStageChoices[] = {3, 4, 5, 6, 8};
   SmallmPlan best;
   double best_cost = -1.0;
@@ -432,7 +434,7 @@ SmallmPlan plan_smallm(const DeviceInfo& d, int64_t M, int64_t N, int64_t K,
   bool best_one_wave = false;
   for (int g = 1; g <= sm::max_groups(MT); ++g) {
     if (want_groups && g != want_groups) continue;
-    const int regs = d.smallm_regs[CV][MT][g];
+    const int regs = d.smallm_regs[W == 4][CV][MT][g];
     if (regs <= 0) continue;
     const int64_t rows_per_cta = swiglu ? 8 * g : 16 * g;
     const int64_t row_blocks = (unit_rows + rows_per_cta - 1) / rows_per_cta;
@@ -474,7 +476,7 @@ SmallmPlan plan_smallm(const DeviceInfo& d, int64_t M, int64_t N, int64_t K,
   return best;
 }
 
-template <int MT, int CV>
+template <int MT, int CV, int W = sm::kWays>
 int launch_smallm(const DeviceInfo& d, const void* x, const uint8_t* wp, const uint8_t* ws,
                   float gs, float gs_up, void* y, int64_t M, int64_t N, int64_t K, unsigned int flags,
                   cudaStream_t stream, const SegSpec* segs,
@@ -483,7 +485,7 @@ int launch_smallm(const DeviceInfo& d, const void* x, const uint8_t* wp, const u
   const bool swiglu = flags & NVFP4_FLAG_SWIGLU;
   static PlanMemo<SmallmPlan> memo;
   const SmallmPlan plan =
-      memo.get(d, M, N, K, flags, [&] { return plan_smallm<MT, CV>(d, M, N, K, flags); });
+      memo.get(d, M, N, K, flags, [&] { return plan_smallm<MT, CV, W>(d, M, N, K, flags); });
   if (plan.groups == 0) return NVFP4_ERR_INVALID;   // overrides that cannot run
   const int half_rows = 8 * plan.groups;
   CUtensorMap tw, ts, tx;
@@ -521,7 +523,7 @@ int launch_smallm(const DeviceInfo& d, const void* x, const uint8_t* wp, const u
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof cfg);
   cfg.gridDim = dim3(static_cast<unsigned>(plan.row_blocks), static_cast<unsigned>(plan.split), 1);
-  cfg.blockDim = dim3(sm::threads_for(CV), 1, 1);
+  cfg.blockDim = dim3(sm::threads_for(CV, W), 1, 1);
   cfg.dynamicSmemBytes = p.lay.total;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
@@ -536,7 +538,7 @@ int launch_smallm(const DeviceInfo& d, const void* x, const uint8_t* wp, const u
   cfg.attrs = attr;
   cfg.numAttrs = 2;
   const cudaError_t e =
-      cudaLaunchKernelEx(&cfg, smallm_fn<MT, CV>(plan.groups), tw, ts, tx, p);
+      cudaLaunchKernelEx(&cfg, smallm_fn<MT, CV, W>(plan.groups), tw, ts, tx, p);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return NVFP4_ERR_LAUNCH;
@@ -864,7 +866,11 @@ int run(const void* x, const uint8_t* wp, const uint8_t* ws, float gs, float gs_
         if (M == 4)
           return launch_smallm<1, 2>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs, y_host);
         return launch_smallm<1, 4>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs, y_host);
-      case 2: return launch_smallm<2, 0>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs, y_host);
+      // M = 9..16: sixteen consumer warps (two 8-row activation tiles each
+      // leave them half the accumulators of eight): 16.0 us against 16.6
+      // on 8192 x 5120 at M = 16 (and no gain at M = 17..32, which keep
+      // eight)
+      case 2: return launch_smallm<2, 0, 4>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs, y_host);
       case 3: return launch_smallm<3, 0>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs, y_host);
       default: return launch_smallm<4, 0>(*d, x, wp, ws, gs, gs_up, y, M, N, K, flags, stream, segs, y_host);
     }

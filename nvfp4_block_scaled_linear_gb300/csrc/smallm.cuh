@@ -56,17 +56,23 @@ constexpr int kGroupRows = 16;        // rows of one MMA row group
 constexpr int kMaxGroups = 8;         // up to 128 weight rows per CTA
 constexpr int kStageK = 256;          // k per pipeline stage
 constexpr int kKQuarters = 4;         // 64-k quarters of a stage
-constexpr int kConsumerWarps = 8;     // (k quarter, row-group parity)
+constexpr int kWays = 2;              // row-group ways of the default layout
 constexpr int kMaxSplit = 16;         // cluster size limit (non-portable above 8)
 constexpr int kF16MaxRows = 8;        // the f16 path serves M <= 8
 
+// Consumer warps: (k quarter, row-group way) for `ways` row-group ways.
+__host__ __device__ constexpr int consumer_warps(int ways) { return kKQuarters * ways; }
 // Consumers, the TMA producer and (f16 path) cv activation converters.
-__host__ __device__ constexpr int threads_for(int cv) { return (kConsumerWarps + 1 + cv) * 32; }
+__host__ __device__ constexpr int threads_for(int cv, int ways = kWays) {
+  return (consumer_warps(ways) + 1 + cv) * 32;
+}
 
 // Row groups one consumer warp may hold: all of its accumulators live in
 // registers, so the widest activation tiles get fewer.
-__host__ __device__ constexpr int groups_per_warp(int mt) { return mt <= 2 ? 4 : 2; }
-__host__ __device__ constexpr int max_groups(int mt) { return 2 * groups_per_warp(mt); }
+__host__ __device__ constexpr int max_groups(int mt) { return mt <= 2 ? 8 : 4; }
+__host__ __device__ constexpr int groups_per_warp(int mt, int ways = kWays) {
+  return max_groups(mt) / ways;
+}
 
 // Shared-memory layout of one launch (byte offsets from the 1024-aligned
 // base), computed on the host per call.  Stage: packed weights
@@ -221,18 +227,23 @@ __device__ __noinline__ void flagged_rows_bf16(const uint8_t* st, uint32_t mine,
 
 // CV: 0 for the bf16 path; 1, 2 or 4 for the f16 path with that many
 // activation converter warps (the host picks more as M grows).
-template <int MT, int G, int CV>
-__global__ void __launch_bounds__(threads_for(CV), CV > 0 ? 2 : 1)
+// W: row-group ways -- 4 * W consumer warps, warp (k quarter, way w) taking
+// the row groups w, w + W, ... of the CTA (2: eight consumers; 4: sixteen,
+// for the bf16 path, with a quarter of the accumulators each).
+template <int MT, int G, int CV, int W = kWays>
+__global__ void __launch_bounds__(threads_for(CV, W), CV > 0 ? 2 : 1)
     smallm_kernel(const __grid_constant__ CUtensorMap tm_w,
                   const __grid_constant__ CUtensorMap tm_s,
                   const __grid_constant__ CUtensorMap tm_x, const Params p) {
   constexpr bool F16 = CV > 0;
-  constexpr int kThreads = threads_for(CV);
-  constexpr int RG = groups_per_warp(MT);
+  constexpr int kThreads = threads_for(CV, W);
+  constexpr int kConsumerWarps = consumer_warps(W);
+  constexpr int RG = groups_per_warp(MT, W);
   constexpr int C = MT * 8;
   constexpr int rows = G * kGroupRows;
   constexpr int half_rows = rows / 2;
   static_assert(G >= 1 && G <= max_groups(MT), "row groups per CTA out of range");
+  static_assert(W == kWays || !F16, "the f16 path keeps the default consumer layout");
   static_assert(!F16 || MT == 1, "the f16 path serves M <= 8");
   const SmemLayout& L = p.lay;
   extern __shared__ uint8_t smem_raw[];
@@ -477,8 +488,8 @@ __global__ void __launch_bounds__(threads_for(CV), CV > 0 ? 2 : 1)
     asm volatile("bar.arrive 2, %0;" ::"n"((kConsumerWarps + CV) * 32) : "memory");
   } else if (warp < kConsumerWarps) {
     // ------------------------------------------------------------ consumers
-    // warp = (k quarter kq, row-group parity rp): 64 k of every stage for
-    // the row groups rp, rp+2, ... of this CTA.
+    // warp = (k quarter kq, row-group way rp): 64 k of every stage for
+    // the row groups rp, rp + W, ... of this CTA.
     const int kq = warp & 3, rp = warp >> 2;
     const int g = lane >> 2, t = lane & 3;
     float acc[RG][MT][4];
@@ -578,14 +589,14 @@ __global__ void __launch_bounds__(threads_for(CV), CV > 0 ? 2 : 1)
 
 #pragma unroll
       for (int i = 0; i < RG; ++i) {
-        const int r = rp + 2 * i;
-        if (r >= G) break;                       // uniform across the warp
+        const int r = rp + W * i;
+        if (G != W * RG && r >= G) break;        // uniform; never when G fills the ways
         const uint2 wa =
-            *reinterpret_cast<const uint2*>(st + w_base[0] + i * 2 * kGroupRows * 128);
+            *reinterpret_cast<const uint2*>(st + w_base[0] + i * W * kGroupRows * 128);
         const uint2 wb =
-            *reinterpret_cast<const uint2*>(st + w_base[1] + i * 2 * kGroupRows * 128);
-        const uint32_t sa = lut[st[s_base[0] + i * 2 * kGroupRows * 16]];
-        const uint32_t sb = lut[st[s_base[1] + i * 2 * kGroupRows * 16]];
+            *reinterpret_cast<const uint2*>(st + w_base[1] + i * W * kGroupRows * 128);
+        const uint32_t sa = lut[st[s_base[0] + i * W * kGroupRows * 16]];
+        const uint32_t sb = lut[st[s_base[1] + i * W * kGroupRows * 16]];
         uint32_t pa[8], pb[8];
         if (F16) {
           dequant8_f16(wa.x, sa, &pa[0]);
@@ -635,8 +646,8 @@ __global__ void __launch_bounds__(threads_for(CV), CV > 0 ? 2 : 1)
     float* red = reinterpret_cast<float*>(smem);
 #pragma unroll
     for (int i = 0; i < RG; ++i) {
-      const int r = rp + 2 * i;
-      if (r >= G) break;
+      const int r = rp + W * i;
+      if (G != W * RG && r >= G) break;
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) {
         const int ra = kGroupRows * r + 2 * g, col = mt * 8 + 2 * t;
