@@ -455,8 +455,11 @@ SmallmPlan plan_smallm(const DeviceInfo& d, int64_t M, int64_t N, int64_t K,
         double cost = static_cast<double>(per_sm) * g * ((T + s - 1) / s + 2);
         if (in_flight < kWantInFlight) cost *= kWantInFlight / in_flight;
         // A lone CTA on an SM issues ~26% slower than two sharing it (fewer
-        // warps to hide latency; measured on the decode shape).
-        if (std::min<int64_t>(per_sm, occ) < 2) cost /= kLoneCtaEfficiency;
+        // warps to hide latency; measured on the decode shape).  Not so for
+        // three or four 8-row activation tiles (M = 17..32): q/k/v at M = 32
+        // (8192 x 5120) takes 18.3 us with 128 lone CTAs against 20.5 us with
+        // two CTAs per SM and a split of 2.
+        if (MT <= 2 && std::min<int64_t>(per_sm, occ) < 2) cost /= kLoneCtaEfficiency;
         const bool better =
             best_cost < 0 || (one_wave && !best_one_wave) ||
             (one_wave == best_one_wave &&

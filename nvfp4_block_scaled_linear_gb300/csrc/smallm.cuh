@@ -247,8 +247,9 @@ __global__ void __launch_bounds__(threads_for(CV, W), CV > 0 ? 2 : 1)
   static_assert(!F16 || MT == 1, "the f16 path serves M <= 8");
   const SmemLayout& L = p.lay;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  // 1024-aligned base, formed by arithmetic on the shared array itself so
+  // that every access through it stays a shared-memory access
+  uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   uint32_t* lut = reinterpret_cast<uint32_t*>(smem + L.lut_off);
   float* part = reinterpret_cast<float*>(smem + L.part_off);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + L.bar_off);

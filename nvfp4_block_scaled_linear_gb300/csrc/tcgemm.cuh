@@ -88,8 +88,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const __grid_constant__ CUtensorMap tm_w,
                   const __grid_constant__ CUtensorMap tm_s, const Params p) {
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  // 1024-aligned base, formed by arithmetic on the shared array itself so
+  // that every access through it stays a shared-memory access
+  uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   uint32_t* lut = reinterpret_cast<uint32_t*>(smem + kLutOff);
   uint64_t* tma_full = reinterpret_cast<uint64_t*>(smem + kBarOff);
   uint64_t* a_full = tma_full + kStages;
