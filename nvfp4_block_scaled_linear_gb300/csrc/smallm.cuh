@@ -539,7 +539,9 @@ __global__ void __launch_bounds__(threads_for(CV, W), CV > 0 ? 2 : 1)
     int slot = 0;
     uint32_t par = 0;
     for (int it = 0; it < n_stages; ++it, slot = next_slot(slot, L.stages, par)) {
-      if (!mbar_wait(&full[slot], par, abort_flag, p.wait_ns)) break;
+      // f16 path: the converter waited for the copies before releasing the
+      // stage, so its barrier alone orders them before the loads below
+      if (!F16 && !mbar_wait(&full[slot], par, abort_flag, p.wait_ns)) break;
       if (F16 && !mbar_wait(&conv[slot], par, abort_flag, p.wait_ns)) break;
       const uint8_t* st = smem + slot * L.stage_bytes;
 
@@ -588,17 +590,14 @@ __global__ void __launch_bounds__(threads_for(CV, W), CV > 0 ? 2 : 1)
         }
       }
 
-#pragma unroll
-      for (int i = 0; i < RG; ++i) {
-        const int r = rp + W * i;
-        if (G != W * RG && r >= G) break;        // uniform; never when G fills the ways
+      // one row group: its weights dequantised, then its MMA chain
+      auto group_operands = [&](int i, uint32_t (&pa)[8], uint32_t (&pb)[8]) {
         const uint2 wa =
             *reinterpret_cast<const uint2*>(st + w_base[0] + i * W * kGroupRows * 128);
         const uint2 wb =
             *reinterpret_cast<const uint2*>(st + w_base[1] + i * W * kGroupRows * 128);
         const uint32_t sa = lut[st[s_base[0] + i * W * kGroupRows * 16]];
         const uint32_t sb = lut[st[s_base[1] + i * W * kGroupRows * 16]];
-        uint32_t pa[8], pb[8];
         if (F16) {
           dequant8_f16(wa.x, sa, &pa[0]);
           dequant8_f16(wa.y, sa, &pa[4]);
@@ -610,17 +609,41 @@ __global__ void __launch_bounds__(threads_for(CV, W), CV > 0 ? 2 : 1)
           dequant8_strided(wb.x, sb, &pb[0]);
           dequant8_strided(wb.y, sb, &pb[4]);
         }
+      };
+      auto group_mma = [&](int i, int s, const uint32_t (&pa)[8], const uint32_t (&pb)[8]) {
 #pragma unroll
-        for (int s = 0; s < 4; ++s)
+        for (int mt = 0; mt < MT; ++mt) {
+          if (F16)
+            mma_f16_16816(acc[i][mt], pa[2 * s], pb[2 * s], pa[2 * s + 1], pb[2 * s + 1],
+                          bx[mt][2 * s], bx[mt][2 * s + 1]);
+          else
+            mma_bf16_16816(acc[i][mt], pa[2 * s], pb[2 * s], pa[2 * s + 1], pb[2 * s + 1],
+                           bx[mt][2 * s], bx[mt][2 * s + 1]);
+        }
+      };
+      if constexpr (G == W * RG && RG % 2 == 0) {
+        // a full CTA: two groups at a time, their MMA chains interleaved
 #pragma unroll
-          for (int mt = 0; mt < MT; ++mt) {
-            if (F16)
-              mma_f16_16816(acc[i][mt], pa[2 * s], pb[2 * s], pa[2 * s + 1], pb[2 * s + 1],
-                            bx[mt][2 * s], bx[mt][2 * s + 1]);
-            else
-              mma_bf16_16816(acc[i][mt], pa[2 * s], pb[2 * s], pa[2 * s + 1], pb[2 * s + 1],
-                             bx[mt][2 * s], bx[mt][2 * s + 1]);
+        for (int i = 0; i < RG; i += 2) {
+          uint32_t pa0[8], pb0[8], pa1[8], pb1[8];
+          group_operands(i, pa0, pb0);
+          group_operands(i + 1, pa1, pb1);
+#pragma unroll
+          for (int s4 = 0; s4 < 4; ++s4) {
+            group_mma(i, s4, pa0, pb0);
+            group_mma(i + 1, s4, pa1, pb1);
           }
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < RG; ++i) {
+          const int r = rp + W * i;
+          if (G != W * RG && r >= G) break;      // uniform; never when G fills the ways
+          uint32_t pa[8], pb[8];
+          group_operands(i, pa, pb);
+#pragma unroll
+          for (int s4 = 0; s4 < 4; ++s4) group_mma(i, s4, pa, pb);
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[slot]);
