@@ -450,8 +450,14 @@ SmallmPlan plan_smallm(const DeviceInfo& d, int64_t M, int64_t N, int64_t K,
         const int64_t ctas = row_blocks * s;
         const bool one_wave = ctas <= slots;
         const int64_t per_sm = (ctas + d.num_sms - 1) / d.num_sms;
-        const double in_flight = static_cast<double>(std::min<int64_t>(per_sm, occ)) *
-                                 (stages - 1) * g * kGroupBytesPerStage;
+        // bytes a stage brings: the weights and scales of its g groups and,
+        // with four 8-row activation tiles (16 KB a stage, more than most
+        // CTAs' weights), the activations: o at M = 32 (5120 x 6144) 19.9 ->
+        // 17.9 us, 1024 x 4096 17.7 -> 7.3; counting them at M = 17..24 as
+        // well cost 2-9%
+        const double stage_bytes = g * kGroupBytesPerStage + (MT == 4 ? lay.x_tx : 0);
+        const double in_flight =
+            static_cast<double>(std::min<int64_t>(per_sm, occ)) * (stages - 1) * stage_bytes;
         double cost = static_cast<double>(per_sm) * g * ((T + s - 1) / s + 2);
         if (in_flight < kWantInFlight) cost *= kWantInFlight / in_flight;
         // A lone CTA on an SM issues ~26% slower than two sharing it (fewer
