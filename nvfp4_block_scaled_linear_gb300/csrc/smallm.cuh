@@ -89,13 +89,22 @@ struct SmemLayout {
   int x_tx;         // activation bytes a stage receives
   int x16_off;      // f16 activation tile, within a stage (f16 path)
   int exp_off;      // int[8] activation exponents, within a stage (f16 path)
-  int part_off;     // CTA partials [16G][MT*8] f32
+  int part_off;     // CTA partials [MT*8][16G + kRedPad] f32
   int lut_off;      // 256 scale pairs
   int bar_off;      // full[stages], conv[stages], empty[stages], abort flag
   int total;        // dynamic shared memory to request (includes alignment slack)
 };
 
 __host__ __device__ constexpr int align_up(int v, int a) { return (v + a - 1) / a * a; }
+
+// Partial sums in shared memory are column-major, [activation row m][weight
+// row j] with a row pitch of 16G + kRedPad floats: the warps' paired stores
+// (weight rows ra, ra + 1 of one column) then take the minimum two
+// wavefronts, and the readers (consecutive j) none more than one.
+constexpr int kRedPad = 8;
+__host__ __device__ constexpr int red_pitch(int groups) {
+  return groups * kGroupRows + kRedPad;
+}
 
 __host__ __device__ constexpr SmemLayout make_layout(int mt, int groups, int stages,
                                                      bool f16, int m_rows) {
@@ -121,7 +130,7 @@ __host__ __device__ constexpr SmemLayout make_layout(int mt, int groups, int sta
   }
   l.stage_bytes = align_up(end, 1024);
   l.part_off = stages * l.stage_bytes;
-  l.lut_off = l.part_off + groups * kGroupRows * mt * 8 * 4;
+  l.lut_off = l.part_off + mt * 8 * red_pitch(groups) * 4;
   l.bar_off = l.lut_off + 256 * 4;
   l.total = l.bar_off + 3 * stages * 8 + 16 + 1024;
   return l;
@@ -129,7 +138,7 @@ __host__ __device__ constexpr SmemLayout make_layout(int mt, int groups, int sta
 
 // The cross-warp reduction reuses the ring; it must fit.
 __host__ __device__ constexpr bool layout_ok(const SmemLayout& l, int mt, int groups) {
-  return kKQuarters * groups * kGroupRows * mt * 8 * 4 <= l.stages * l.stage_bytes;
+  return kKQuarters * mt * 8 * red_pitch(groups) * 4 <= l.stages * l.stage_bytes;
 }
 
 struct Params {
@@ -154,6 +163,26 @@ struct Params {
 // 2^a as fp32, a in [-126, 127].
 __device__ __forceinline__ float pow2f(int a) { return __int_as_float((a + 127) << 23); }
 
+// Output (m, n) from its accumulated sums: v (row n, or the gate row with
+// SwiGLU) and u (the up row), both before the global scale.  Columns past
+// the output width (the last CTA's padding rows) are skipped.
+__device__ __forceinline__ void store_output(const Params& p, int m, int64_t n, float v,
+                                             float u) {
+  const int64_t n_out = p.swiglu ? p.N / 2 : p.N;
+  if (n >= n_out) return;
+  float yv = v * (p.seg.n ? seg_scale(p.seg, n) : p.out_scale);
+  if (p.swiglu) yv = silu_mul(yv, u * p.out_scale_up);
+  const int64_t off = static_cast<int64_t>(m) * n_out + n;
+  if (p.out_f32) {
+    static_cast<float*>(p.y)[off] = yv;
+    if (p.y_host) static_cast<float*>(p.y_host)[off] = yv;
+  } else {
+    const __nv_bfloat16 yb = __float2bfloat16_rn(yv);
+    static_cast<__nv_bfloat16*>(p.y)[off] = yb;
+    if (p.y_host) static_cast<__nv_bfloat16*>(p.y_host)[off] = yb;
+  }
+}
+
 // Next position in a ring of `stages` slots; flips the barrier parity on
 // wrap-around.
 __device__ __forceinline__ int next_slot(int slot, int stages, uint32_t& parity) {
@@ -169,7 +198,7 @@ __device__ __forceinline__ int next_slot(int slot, int stages, uint32_t& parity)
 // the consumers' bf16 path -- weights code * scale * 2^-10, activations as
 // given, paired (k, k+4) -- over all 16G rows and 256 k of the stage.  The
 // sums of the flagged rows' columns are added to the CTA's partials
-// [16G rows][8] (still carrying 2^-10; the consumers' reduction scales them
+// [8][16G + kRedPad] (still carrying 2^-10; the consumers' reduction scales them
 // by 2^10); other columns stay zero and are not written.  Slow (about the
 // consumers' whole stage in one warp), taken only for rows outside the f16
 // window, and kept out of line so that it costs the converter's loop nothing
@@ -177,7 +206,7 @@ __device__ __forceinline__ int next_slot(int slot, int stages, uint32_t& parity)
 template <int G>
 __device__ __noinline__ void flagged_rows_bf16(const uint8_t* st, uint32_t mine,
                                                const SmemLayout& L, float* part, int lane) {
-  constexpr int C = 8;
+  constexpr int P = red_pitch(G);
   const int g = lane >> 2, t = lane & 3;
   const bool col_g = (mine >> g) & 1u;                  // B column g
   const bool own0 = (mine >> (2 * t)) & 1u;             // D columns 2t, 2t + 1
@@ -215,12 +244,12 @@ __device__ __noinline__ void flagged_rows_bf16(const uint8_t* st, uint32_t mine,
     }
     const int ra = kGroupRows * r + 2 * g;
     if (own0) {
-      part[ra * C + 2 * t] += d[0];
-      part[(ra + 1) * C + 2 * t] += d[2];
+      part[2 * t * P + ra] += d[0];
+      part[2 * t * P + ra + 1] += d[2];
     }
     if (own1) {
-      part[ra * C + 2 * t + 1] += d[1];
-      part[(ra + 1) * C + 2 * t + 1] += d[3];
+      part[(2 * t + 1) * P + ra] += d[1];
+      part[(2 * t + 1) * P + ra + 1] += d[3];
     }
   }
 }
@@ -242,6 +271,7 @@ __global__ void __launch_bounds__(threads_for(CV, W), CV > 0 ? 2 : 1)
   constexpr int C = MT * 8;
   constexpr int rows = G * kGroupRows;
   constexpr int half_rows = rows / 2;
+  constexpr int P = red_pitch(G);
   static_assert(G >= 1 && G <= max_groups(MT), "row groups per CTA out of range");
   static_assert(W == kWays || !F16, "the f16 path keeps the default consumer layout");
   static_assert(!F16 || MT == 1, "the f16 path serves M <= 8");
@@ -280,7 +310,7 @@ __global__ void __launch_bounds__(threads_for(CV, W), CV > 0 ? 2 : 1)
   // f16 path: the converters add the bf16 products of flagged rows into the
   // CTA's partials during the loop (the consumers' sums join them after it)
   if (F16)
-    for (int i = threadIdx.x; i < rows * C; i += kThreads) part[i] = 0.f;
+    for (int i = threadIdx.x; i < C * P; i += kThreads) part[i] = 0.f;
   if (threadIdx.x == 0) {
     for (int s = 0; s < L.stages; ++s) {
       mbar_init(&full[s], 1);
@@ -662,11 +692,13 @@ __global__ void __launch_bounds__(threads_for(CV, W), CV > 0 ? 2 : 1)
 
     // Warp partials -> ring (free now: every stage has been consumed once
     // all consumer warps -- and, on the f16 path, the converters, which read
-    // the ring for flagged rows -- pass the barrier below).
+    // the ring for flagged rows -- pass the barrier below).  Only the
+    // columns that hold activation rows are kept.
     if (F16)
       asm volatile("bar.sync 2, %0;" ::"n"((kConsumerWarps + CV) * 32) : "memory");
     else
       asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+    const int M = static_cast<int>(p.M);
     float* red = reinterpret_cast<float*>(smem);
 #pragma unroll
     for (int i = 0; i < RG; ++i) {
@@ -675,34 +707,57 @@ __global__ void __launch_bounds__(threads_for(CV, W), CV > 0 ? 2 : 1)
 #pragma unroll
       for (int mt = 0; mt < MT; ++mt) {
         const int ra = kGroupRows * r + 2 * g, col = mt * 8 + 2 * t;
-        float* base = red + kq * rows * C;
-        base[ra * C + col] = acc[i][mt][0];
-        base[ra * C + col + 1] = acc[i][mt][1];
-        base[(ra + 1) * C + col] = acc[i][mt][2];
-        base[(ra + 1) * C + col + 1] = acc[i][mt][3];
+        float* base = red + kq * C * P + ra;
+        if (col < M)
+          *reinterpret_cast<float2*>(base + col * P) = make_float2(acc[i][mt][0], acc[i][mt][2]);
+        if (col + 1 < M)
+          *reinterpret_cast<float2*>(base + (col + 1) * P) =
+              make_float2(acc[i][mt][1], acc[i][mt][3]);
       }
     }
     asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
-    for (int i = threadIdx.x; i < rows * C; i += kConsumerWarps * 32) {
+    // the four k quarters' sums of (weight row j, activation row m), and on
+    // the f16 path the flagged rows' bf16 products (carrying 2^-10)
+    auto quarter_sum = [&](int j, int m) {
       float s = 0.f;
 #pragma unroll
-      for (int q = 0; q < kKQuarters; ++q) s += red[q * rows * C + i];
-      // f16 path: plus the flagged rows' bf16 products (carrying 2^-10)
-      part[i] = F16 ? s + part[i] * kWeightPow2 : s;
+      for (int q = 0; q < kKQuarters; ++q) s += red[(q * C + m) * P + j];
+      return F16 ? s + part[m * P + j] * kWeightPow2 : s;
+    };
+    if (split == 1) {
+      // the CTA holds whole sums: write the outputs from here
+      if (*abort_flag && threadIdx.x == 0) atomicOr(p.err, kErrWaitTimeout);
+      if (p.swiglu) {
+        const int64_t n_base = static_cast<int64_t>(blockIdx.x) * half_rows;
+        for (int i = threadIdx.x; i < half_rows * M; i += kConsumerWarps * 32) {
+          const int m = i / half_rows, j = i % half_rows;
+          store_output(p, m, n_base + j, quarter_sum(j, m), quarter_sum(half_rows + j, m));
+        }
+      } else {
+        const int64_t n_base = static_cast<int64_t>(blockIdx.x) * rows;
+        for (int i = threadIdx.x; i < rows * M; i += kConsumerWarps * 32) {
+          const int m = i / rows, j = i % rows;
+          store_output(p, m, n_base + j, quarter_sum(j, m), 0.f);
+        }
+      }
+      return;
+    }
+    for (int i = threadIdx.x; i < rows * M; i += kConsumerWarps * 32) {
+      const int m = i / rows, j = i % rows;
+      part[m * P + j] = quarter_sum(j, m);
     }
   }
 
+  if (split == 1) return;             // producer and converters: nothing left
   if (*abort_flag && threadIdx.x == 0) atomicOr(p.err, kErrWaitTimeout);
 
   // ---------------------------------------------------------------- epilogue
-  // Every CTA of the cluster finishes its partial; CTA z then reduces a
-  // 1/split share of the outputs across the cluster's shared memories.
-  // (Reconverge each warp first: the cluster barrier is a warp-aligned op.)
+  // (k split) Every CTA of the cluster finishes its partial; CTA z then
+  // reduces a 1/split share of the outputs across the cluster's shared
+  // memories.  (Reconverge each warp first: the cluster barrier is a
+  // warp-aligned op.)
   __syncwarp();
-  if (split > 1)
-    cluster_sync();
-  else
-    __syncthreads();
+  cluster_sync();
   {
     const int M = static_cast<int>(p.M);
     const int R = p.swiglu ? half_rows : rows;           // outputs per activation row
@@ -710,37 +765,18 @@ __global__ void __launch_bounds__(threads_for(CV, W), CV > 0 ? 2 : 1)
     const int i0 = static_cast<int>((int64_t)items * z / split);
     const int i1 = static_cast<int>((int64_t)items * (z + 1) / split);
     const uint32_t part_local = smem_addr(part);
-    const int64_t n_out = p.swiglu ? p.N / 2 : p.N;
     const int64_t n_base = static_cast<int64_t>(blockIdx.x) * R;
     for (int i = i0 + threadIdx.x; i < i1; i += kThreads) {
       const int m = i / R, j = i % R;
-      if (n_base + j >= n_out) continue;
-      float v = 0.f, u = 0.f;
-      if (split == 1) {
-        v = part[j * C + m];
-        if (p.swiglu) u = part[(half_rows + j) * C + m];
-      } else {
-        v = cluster_sum_f32<kMaxSplit>(part_local, 4u * (j * C + m), split);
-        if (p.swiglu)
-          u = cluster_sum_f32<kMaxSplit>(part_local, 4u * ((half_rows + j) * C + m), split);
-      }
-      float yv = v * (p.seg.n ? seg_scale(p.seg, n_base + j) : p.out_scale);
-      if (p.swiglu) yv = silu_mul(yv, u * p.out_scale_up);
-      const int64_t off = static_cast<int64_t>(m) * n_out + n_base + j;
-      if (p.out_f32) {
-        static_cast<float*>(p.y)[off] = yv;
-        if (p.y_host) static_cast<float*>(p.y_host)[off] = yv;
-      } else {
-        const __nv_bfloat16 yb = __float2bfloat16_rn(yv);
-        static_cast<__nv_bfloat16*>(p.y)[off] = yb;
-        if (p.y_host) static_cast<__nv_bfloat16*>(p.y_host)[off] = yb;
-      }
+      const float v = cluster_sum_f32<kMaxSplit>(part_local, 4u * (m * P + j), split);
+      const float u =
+          p.swiglu ? cluster_sum_f32<kMaxSplit>(part_local, 4u * (m * P + half_rows + j), split)
+                   : 0.f;
+      store_output(p, m, n_base + j, v, u);
     }
   }
-  if (split > 1) {
-    __syncwarp();
-    cluster_sync();   // keep every partial alive until all readers are done
-  }
+  __syncwarp();
+  cluster_sync();   // keep every partial alive until all readers are done
 }
 
 }  // namespace smallm
