@@ -10,12 +10,14 @@
 //    the 64 matching up rows) and a contiguous range of k.  A producer warp
 //    streams 256-k stages -- packed codes (128B-swizzled), block scales and
 //    the activations -- into a shared-memory ring with TMA.  The activation
-//    tile is the MMA's B operand as it lands: bf16, 128B-swizzled K-major,
-//    NM = 16 or 32 rows, the rows past M filled with zeros by the copy.
+//    tile is the MMA's B operand: bf16, 128B-swizzled K-major, NM = 16 or
+//    32 rows, the rows past M filled with zeros by the copy.
 //  * A stage is four 64-k jobs.  Job j goes to lane group j mod NI: four
 //    dequantisation warps (one per 32-row TMEM lane quadrant) write the
 //    job's weights as bf16 code * scale * 2^-10 (exact) into that group's
-//    TMEM ring, and the group's own MMA issuer adds A (TMEM) x B (shared
+//    TMEM ring, with the k of every 8-k block in the order the bit trick
+//    yields them, and permute the job's activation tile in place to the same
+//    order; the group's own MMA issuer then adds A (TMEM) x B (shared
 //    memory) into the group's own fp32 accumulator in TMEM.  NI issuers run
 //    side by side: one thread issues at most one tcgen05.mma every
 //    ~30-60 ns, far below what the tensor core accepts from several.
@@ -92,9 +94,14 @@ __host__ __device__ constexpr SmemLayout make_layout(int nm, int ni, int stages)
   return l;
 }
 
+// The CTA's partial [128 rows][NM] lives in the ring with a row pitch of
+// NM + 1 floats: a warp's stores (one row per thread) and the epilogue's
+// loads (consecutive rows) then fall in distinct banks.
+__host__ __device__ constexpr int part_pitch(int nm) { return nm + 1; }
+
 // The final exchange reuses the ring; it must fit.
 __host__ __device__ constexpr bool layout_ok(const SmemLayout& l, int nm) {
-  return l.stages >= 2 && kRows * nm * 4 <= l.stages * l.stage_bytes;
+  return l.stages >= 2 && kRows * part_pitch(nm) * 4 <= l.stages * l.stage_bytes;
 }
 
 struct Params {
@@ -143,6 +150,7 @@ __global__ void __launch_bounds__(Roles<NM, NI>::kThreads, Roles<NM, NI>::kCtasP
   static_assert(NM == 16 || NM == 32, "MMA N is 16 or 32");
   using R = Roles<NM, NI>;
   constexpr int kThreads = R::kThreads;
+  constexpr int kPitch = part_pitch(NM);
   const SmemLayout& L = p.lay;
   const int S = L.stages;
   extern __shared__ uint8_t smem_raw[];
@@ -311,7 +319,9 @@ __global__ void __launch_bounds__(Roles<NM, NI>::kThreads, Roles<NM, NI>::kCtasP
     // ------------------------------------------------------------ dequantisers
     // Warp (lane group gi, quadrant qd): lane = weight row 32 qd + lane = its
     // TMEM lane; for each job of the group it writes the row's 64 k as 32
-    // bf16 pairs (k 2c, 2c+1 in column c) into the group's next TMEM slot.
+    // bf16 pairs into the group's next TMEM slot: column 4i + p holds
+    // k = 8i + p and 8i + p + 4, the order the bit trick yields (the job's
+    // activations are permuted to match).
     const int dw = warp - R::kWarpDeq;
     const int gi = dw >> 2, qd = warp & 3;
     const int row = 32 * qd + lane;
@@ -327,7 +337,25 @@ __global__ void __launch_bounds__(Roles<NM, NI>::kThreads, Roles<NM, NI>::kCtasP
       if (n >= kSlotsPerGroup &&
           !warp_wait(&a_empty[gi * kSlotsPerGroup + aslot], epar, abort_flag))
         break;          // the slot's previous job (kSlotsPerGroup jobs back) not done
-      const uint8_t* st = smem + slot * L.stage_bytes;
+      uint8_t* st = smem + slot * L.stage_bytes;
+      // The job's activations (64 k of NM rows) into the weights' k order:
+      // within every 8 k, (k0, k4, k1, k5, k2, k6, k3, k7).  Both MMA
+      // operands then list the k of each 8-k block in that same order, which
+      // leaves every product and sum of the contraction as it was, and the
+      // weights need no re-pairing after the bit trick.  A 16-byte chunk is 8
+      // consecutive k of one row (the 128B swizzle moves whole chunks), so
+      // the permutation is chunk-local; the job's four warps share it.
+      {
+        uint8_t* xq = st + L.x_off + q * (NM * 128);
+#pragma unroll
+        for (int c = 32 * qd + lane; c < NM * 8; c += 128) {
+          const uint4 v = *reinterpret_cast<const uint4*>(xq + c * 16);
+          *reinterpret_cast<uint4*>(xq + c * 16) =
+              make_uint4(prmt(v.x, v.z, 0x5410u), prmt(v.x, v.z, 0x7632u),
+                         prmt(v.y, v.w, 0x5410u), prmt(v.y, v.w, 0x7632u));
+        }
+        fence_proxy_async_smem();   // the tensor core reads the tile next
+      }
       // 64 k = code chunks 2q, 2q+1 of the row's 128-byte swizzled line
       const uint4 w0 =
           *reinterpret_cast<const uint4*>(st + row * 128 + (((2 * q) ^ (row & 7)) << 4));
@@ -341,11 +369,7 @@ __global__ void __launch_bounds__(Roles<NM, NI>::kThreads, Roles<NM, NI>::kCtasP
       const uint32_t sc[4] = {S0, S1, S2, S3};
       uint32_t out[32];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        uint32_t t[4];
-        dequant8_strided(words[i], sc[i >> 1], t);
-        pair_consecutive(t, &out[4 * i]);
-      }
+      for (int i = 0; i < 8; ++i) dequant8_strided(words[i], sc[i >> 1], &out[4 * i]);
       tc_fence_after_sync();
       tmem_st_32cols(t_lane + (gi * kSlotsPerGroup + aslot) * kSlotCols, out);
       tmem_st_wait();
@@ -392,7 +416,7 @@ __global__ void __launch_bounds__(Roles<NM, NI>::kThreads, Roles<NM, NI>::kCtasP
         }
 #pragma unroll
         for (int c = 0; c < 16; ++c)
-          if (16 * h + c < M) part[row * NM + 16 * h + c] = sum[c];
+          if (16 * h + c < M) part[row * kPitch + 16 * h + c] = sum[c];
       }
     }
   }
@@ -423,15 +447,15 @@ __global__ void __launch_bounds__(Roles<NM, NI>::kThreads, Roles<NM, NI>::kCtasP
     const int64_t n_out = p.swiglu ? p.N / 2 : p.N;
     const int64_t n_base = static_cast<int64_t>(blockIdx.x) * Rn;
     for (int i = i0 + threadIdx.x; i < i1; i += kThreads) {
-      const int m = i / Rn, jr = i % Rn;
+      const int m = i >> (p.swiglu ? 6 : 7), jr = i & (Rn - 1);   // Rn = 64 or 128
       float v = 0.f, u = 0.f;
       if (split == 1) {
-        v = part[jr * NM + m];
-        if (p.swiglu) u = part[(kHalfRows + jr) * NM + m];
+        v = part[jr * kPitch + m];
+        if (p.swiglu) u = part[(kHalfRows + jr) * kPitch + m];
       } else {
-        v = cluster_sum_f32<kMaxSplit>(part_local, 4u * (jr * NM + m), split);
+        v = cluster_sum_f32<kMaxSplit>(part_local, 4u * (jr * kPitch + m), split);
         if (p.swiglu)
-          u = cluster_sum_f32<kMaxSplit>(part_local, 4u * ((kHalfRows + jr) * NM + m), split);
+          u = cluster_sum_f32<kMaxSplit>(part_local, 4u * ((kHalfRows + jr) * kPitch + m), split);
       }
       float yv = v * (p.seg.n ? seg_scale(p.seg, n_base + jr) : p.out_scale);
       if (p.swiglu) yv = silu_mul(yv, u * p.out_scale_up);
