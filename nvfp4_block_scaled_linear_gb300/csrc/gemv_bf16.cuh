@@ -24,8 +24,10 @@
 //  * The accumulators stay in TMEM for the whole k range; the epilogue reads
 //    them once, sums the NI groups and applies 2^10 / global scale.
 //  * Split-K: CTAs that share rows but not k form one thread-block cluster;
-//    partials are reduced across the cluster through distributed shared
-//    memory.  No global workspace, no atomics, no waits on other CTAs.
+//    each CTA owns a share of the outputs, pushes its partial values of the
+//    others' shares into their shared memory (remote stores) and, after one
+//    cluster barrier, sums its own share in rank order.  No global
+//    workspace, no atomics.
 #pragma once
 #include <cstdint>
 #include <cuda_bf16.h>
@@ -99,9 +101,16 @@ __host__ __device__ constexpr SmemLayout make_layout(int nm, int ni, int stages)
 // loads (consecutive rows) then fall in distinct banks.
 __host__ __device__ constexpr int part_pitch(int nm) { return nm + 1; }
 
+// Receive area of the k-split reduction, after the partial: the partial
+// values of this CTA's share of the outputs from every CTA of the cluster,
+// [split][1 or 2][share] floats (two with SwiGLU, whose outputs have half
+// the rows), at most 128 NM + 2 kMaxSplit floats.
+__host__ __device__ constexpr int recv_floats(int nm) { return kRows * nm + 2 * kMaxSplit; }
+
 // The final exchange reuses the ring; it must fit.
 __host__ __device__ constexpr bool layout_ok(const SmemLayout& l, int nm) {
-  return l.stages >= 2 && kRows * part_pitch(nm) * 4 <= l.stages * l.stage_bytes;
+  return l.stages >= 2 &&
+         (kRows * part_pitch(nm) + recv_floats(nm)) * 4 <= l.stages * l.stage_bytes;
 }
 
 struct Params {
@@ -430,49 +439,67 @@ __global__ void __launch_bounds__(Roles<NM, NI>::kThreads, Roles<NM, NI>::kCtasP
   float* part = reinterpret_cast<float*>(smem);
 
   // ---------------------------------------------------------------- epilogue
-  // Every CTA of the cluster finishes its partial; CTA z then reduces a
-  // 1/split share of the outputs across the cluster's shared memories.
-  // (Reconverge each warp first: the cluster barrier is a warp-aligned op.)
-  __syncwarp();
-  if (split > 1)
-    cluster_sync();
-  else
-    __syncthreads();
-  {
-    const int Rn = p.swiglu ? kHalfRows : kRows;           // outputs per activation row
-    const int items = Rn * M;
-    const int i0 = static_cast<int>((int64_t)items * z / split);
-    const int i1 = static_cast<int>((int64_t)items * (z + 1) / split);
-    const uint32_t part_local = smem_addr(part);
+  // Output item i = (activation row i / Rn, weight row i % Rn of the CTA).
+  const int Rn = p.swiglu ? kHalfRows : kRows;           // outputs per activation row
+  const int shift = p.swiglu ? 6 : 7;                    // log2(Rn)
+  const int items = Rn * M;
+  const int nv = p.swiglu ? 2 : 1;                       // partial values per item
+  const int64_t n_base = static_cast<int64_t>(blockIdx.x) * Rn;
+  // value c of item i in this CTA's partial (c = 1: SwiGLU's up row)
+  auto local_part = [&](int i, int c) {
+    return part[((c ? kHalfRows : 0) + (i & (Rn - 1))) * kPitch + (i >> shift)];
+  };
+  auto emit = [&](int i, float v, float u) {
+    const int m = i >> shift, jr = i & (Rn - 1);
     const int64_t n_out = p.swiglu ? p.N / 2 : p.N;
-    const int64_t n_base = static_cast<int64_t>(blockIdx.x) * Rn;
-    for (int i = i0 + threadIdx.x; i < i1; i += kThreads) {
-      const int m = i >> (p.swiglu ? 6 : 7), jr = i & (Rn - 1);   // Rn = 64 or 128
-      float v = 0.f, u = 0.f;
-      if (split == 1) {
-        v = part[jr * kPitch + m];
-        if (p.swiglu) u = part[(kHalfRows + jr) * kPitch + m];
-      } else {
-        v = cluster_sum_f32<kMaxSplit>(part_local, 4u * (jr * kPitch + m), split);
-        if (p.swiglu)
-          u = cluster_sum_f32<kMaxSplit>(part_local, 4u * ((kHalfRows + jr) * kPitch + m), split);
-      }
-      float yv = v * (p.seg.n ? seg_scale(p.seg, n_base + jr) : p.out_scale);
-      if (p.swiglu) yv = silu_mul(yv, u * p.out_scale_up);
-      const int64_t off = static_cast<int64_t>(m) * n_out + n_base + jr;
-      if (p.out_f32) {
-        static_cast<float*>(p.y)[off] = yv;
-        if (p.y_host) static_cast<float*>(p.y_host)[off] = yv;
-      } else {
-        const __nv_bfloat16 yb = __float2bfloat16_rn(yv);
-        static_cast<__nv_bfloat16*>(p.y)[off] = yb;
-        if (p.y_host) static_cast<__nv_bfloat16*>(p.y_host)[off] = yb;
-      }
+    float yv = v * (p.seg.n ? seg_scale(p.seg, n_base + jr) : p.out_scale);
+    if (p.swiglu) yv = silu_mul(yv, u * p.out_scale_up);
+    const int64_t off = static_cast<int64_t>(m) * n_out + n_base + jr;
+    if (p.out_f32) {
+      static_cast<float*>(p.y)[off] = yv;
+      if (p.y_host) static_cast<float*>(p.y_host)[off] = yv;
+    } else {
+      const __nv_bfloat16 yb = __float2bfloat16_rn(yv);
+      static_cast<__nv_bfloat16*>(p.y)[off] = yb;
+      if (p.y_host) static_cast<__nv_bfloat16*>(p.y_host)[off] = yb;
     }
+  };
+  if (split == 1) {
+    __syncthreads();
+    for (int i = threadIdx.x; i < items; i += kThreads)
+      emit(i, local_part(i, 0), p.swiglu ? local_part(i, 1) : 0.f);
+    return;
   }
-  if (split > 1) {
-    __syncwarp();
-    cluster_sync();   // keep every partial alive until all readers are done
+  // k split: CTA z owns the items [begin(z), begin(z + 1)).  Each CTA pushes
+  // its partial values of the other CTAs' items into their receive areas
+  // (remote stores, so no thread waits on a remote round trip), one cluster
+  // barrier makes them visible, and each CTA adds its own items' values in
+  // rank order, from local shared memory.  (Reconverge each warp before a
+  // cluster barrier: it is a warp-aligned op.)
+  auto begin = [&](int r) { return static_cast<int>((int64_t)items * r / split); };
+  const int share_max = (items + split - 1) / split;
+  float* recv = part + kRows * kPitch;                   // [split][nv][share_max]
+  __syncwarp();
+  cluster_sync();     // every partial is final and every ring is free
+  for (int r = 0; r < split; ++r) {
+    if (r == z) continue;
+    const int b = begin(r), e = begin(r + 1);
+    const uint32_t dst = map_to_rank(smem_addr(recv), static_cast<uint32_t>(r));
+    for (int i = b + threadIdx.x; i < e; i += kThreads)
+      for (int c = 0; c < nv; ++c)
+        st_cluster_f32(dst + 4u * static_cast<uint32_t>((z * nv + c) * share_max + (i - b)),
+                       local_part(i, c));
+  }
+  __syncwarp();
+  cluster_sync();     // every push has landed; nothing reads remote memory after this
+  const int b = begin(z), e = begin(z + 1);
+  for (int i = b + threadIdx.x; i < e; i += kThreads) {
+    float v = 0.f, u = 0.f;
+    for (int q = 0; q < split; ++q) {
+      v += q == z ? local_part(i, 0) : recv[(q * nv) * share_max + (i - b)];
+      if (p.swiglu) u += q == z ? local_part(i, 1) : recv[(q * nv + 1) * share_max + (i - b)];
+    }
+    emit(i, v, u);
   }
 }
 

@@ -187,6 +187,10 @@ __device__ __forceinline__ float ld_cluster_f32(uint32_t cluster_addr) {
   return v;
 }
 
+__device__ __forceinline__ void st_cluster_f32(uint32_t cluster_addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(cluster_addr), "f"(v) : "memory");
+}
+
 // Sum, in rank order, of the float at byte offset `off` of the
 // shared-memory object at `local` over CTAs 0..n-1 of the cluster (n <=
 // kMax).  Every remote load is issued before the first add, so that their
