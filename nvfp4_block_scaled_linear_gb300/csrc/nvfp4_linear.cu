@@ -335,16 +335,21 @@ int validate(const void* x, const void* wp, const void* ws, const void* y, int64
 }
 
 // Kernel by M (and, for M = 9..32, the weight size), from graph-timed
-// measurements on GB300: M <= 8 the warp-MMA kernel in f16 (decode 21.8 us
+// measurements on GB300: M <= 8 the warp-MMA kernel in f16 (decode 18.5 us
 // against 29.5-32 us for the tcgen05 few-row kernels); M = 9..32 the bf16
-// tcgen05 few-row kernel on large weight matrices (M = 32: 34816 x 5120 in
-// 53 us against 77 us, 5120 x 17408 in 37 against 51; M = 16: 48 against 55
-// and 33 against 35) and the warp-MMA kernel in bf16 on smaller ones (M = 16,
-// 8192 x 5120: 16 us against 18).  The f16 tcgen05 few-row kernel, 0-6%
-// ahead only at M = 9..12 on the largest shape and up to 1.8x behind
-// elsewhere, runs only when forced.  Every default above M = 8 multiplies
-// the activations exactly (bf16).
-constexpr int64_t kBf16GemvMinWeights = int64_t(1) << 26;
+// tcgen05 few-row kernel on weight matrices of at least kBf16GemvMinWeights(M)
+// and the warp-MMA kernel in bf16 below.  The crossover falls as M grows,
+// the warp MMAs' work growing with M while the tensor core's does not:
+//   M = 12/16: 34816 x 5120 40.7 us against 41.0-41.2 (tcgen05 ahead),
+//              5120 x 17408 27.4-27.8 against 24.5-25.1 (warp MMA ahead);
+//   M = 24:    5120 x 17408 28.2 against 29.2, 12288 x 5120 22.5 against 19.6;
+//   M = 32:    5120 x 6144 14.8 against 16.9, 12288 x 5120 22.8 against 28.7,
+//              8192 x 5120 16.4 against 15.3, 4096 x 4096 10.9 against 9.6.
+// The f16 tcgen05 few-row kernel runs only when forced.  Every default above
+// M = 8 multiplies the activations exactly (bf16).
+constexpr int64_t kBf16GemvMinWeights(int64_t M) {
+  return M <= 16 ? int64_t(1) << 27 : M <= 24 ? int64_t(1) << 26 : int64_t(3) << 23;
+}
 
 int kernel_for(int64_t M, int64_t N, int64_t K, unsigned int flags) {
   if (flags & NVFP4_FLAG_FORCE_SMALLM) return NVFP4_KERNEL_SMALLM;
@@ -352,7 +357,7 @@ int kernel_for(int64_t M, int64_t N, int64_t K, unsigned int flags) {
   if (flags & NVFP4_FLAG_FORCE_GEMV)
     return (flags & NVFP4_FLAG_BF16_MMA) ? NVFP4_KERNEL_GEMV_BF16 : NVFP4_KERNEL_GEMV;
   if (M > kSmallMMax) return NVFP4_KERNEL_TCGEMM;
-  if (M > 8 && N * K >= kBf16GemvMinWeights) return NVFP4_KERNEL_GEMV_BF16;
+  if (M > 8 && N * K >= kBf16GemvMinWeights(M)) return NVFP4_KERNEL_GEMV_BF16;
   return NVFP4_KERNEL_SMALLM;
 }
 

@@ -59,6 +59,9 @@ def test_version_and_status_strings(lib):
     (32, 34816, 5120, 0, _lib.KERNEL_GEMV_BF16),                 # large layer, M = 17..32
     (17, 5120, 17408, 0, _lib.KERNEL_GEMV_BF16),
     (24, 8192, 5120, 0, _lib.KERNEL_SMALLM),                     # N * K < 2^26
+    (16, 5120, 17408, 0, _lib.KERNEL_SMALLM),                    # M <= 16: N * K < 2^27
+    (32, 5120, 6144, 0, _lib.KERNEL_GEMV_BF16),                  # M >= 25: N * K >= 3 * 2^23
+    (32, 4096, 4096, 0, _lib.KERNEL_SMALLM),
     (16, 34816, 5120, 0, _lib.KERNEL_GEMV_BF16),
     (32, 34816, 5120, _lib.FLAG_BF16_MMA, _lib.KERNEL_GEMV_BF16),
     (16, 34816, 5120, _lib.FLAG_BF16_MMA, _lib.KERNEL_GEMV_BF16),
