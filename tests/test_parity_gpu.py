@@ -119,6 +119,18 @@ def test_gemv_bf16_every_split_and_group_count(M):
                            "gemv_bf16 M=%d groups=%d split=%d" % (M, g, s))
 
 
+@pytest.mark.parametrize("M", [9, 32])
+def test_gemv_bf16_swiglu_every_split(M):
+    """The k-split reduction of the bf16 tcgen05 few-row kernel with SwiGLU:
+    two partial values (gate and up row) per output, pushed to the CTA that
+    owns the output, for splits that divide the outputs unevenly."""
+    t = make_linear(M, 640, 4096, seed=1090 + M)
+    for g in (2, 4):
+        for s in (1, 2, 3, 5, 16):
+            full_check(t, _lib.FLAG_SWIGLU | GEMV_BF16 | _lib.FLAG_GROUPS(g) | _lib.FLAG_SPLIT(s),
+                       what="gemv_bf16 swiglu M=%d groups=%d split=%d" % (M, g, s))
+
+
 # ------------------------------------------------------------------ tcgen05
 @pytest.mark.parametrize("M", [33, 64, 255, 256, 257, 600])
 def test_tcgemm_row_counts_and_tails(M):
