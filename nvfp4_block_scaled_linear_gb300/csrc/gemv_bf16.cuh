@@ -104,8 +104,9 @@ __host__ __device__ constexpr int part_pitch(int nm) { return nm + 1; }
 // Receive area of the k-split reduction, after the partial: the partial
 // values of this CTA's share of the outputs from every CTA of the cluster,
 // [split][1 or 2][share] floats (two with SwiGLU, whose outputs have half
-// the rows), at most 128 NM + 2 kMaxSplit floats.
-__host__ __device__ constexpr int recv_floats(int nm) { return kRows * nm + 2 * kMaxSplit; }
+// the rows; shares rounded to even sizes), at most 128 NM + 8 kMaxSplit
+// floats.
+__host__ __device__ constexpr int recv_floats(int nm) { return kRows * nm + 8 * kMaxSplit; }
 
 // The final exchange reuses the ring; it must fit.
 __host__ __device__ constexpr bool layout_ok(const SmemLayout& l, int nm) {
@@ -440,44 +441,55 @@ __global__ void __launch_bounds__(Roles<NM, NI>::kThreads, Roles<NM, NI>::kCtasP
 
   // ---------------------------------------------------------------- epilogue
   // Output item i = (activation row i / Rn, weight row i % Rn of the CTA).
+  // Items go in pairs (i even; Rn is even, so both are of one activation
+  // row): one word stored per pair.
   const int Rn = p.swiglu ? kHalfRows : kRows;           // outputs per activation row
   const int shift = p.swiglu ? 6 : 7;                    // log2(Rn)
   const int items = Rn * M;
   const int nv = p.swiglu ? 2 : 1;                       // partial values per item
   const int64_t n_base = static_cast<int64_t>(blockIdx.x) * Rn;
+  const int64_t n_out = p.swiglu ? p.N / 2 : p.N;
   // value c of item i in this CTA's partial (c = 1: SwiGLU's up row)
   auto local_part = [&](int i, int c) {
     return part[((c ? kHalfRows : 0) + (i & (Rn - 1))) * kPitch + (i >> shift)];
   };
-  auto emit = [&](int i, float v, float u) {
+  // outputs i and i + 1 from their sums v (the row, or SwiGLU's gate row)
+  // and u (SwiGLU's up row), both before the global scale
+  auto emit2 = [&](int i, float v0, float v1, float u0, float u1) {
     const int m = i >> shift, jr = i & (Rn - 1);
-    const int64_t n_out = p.swiglu ? p.N / 2 : p.N;
-    float yv = v * (p.seg.n ? seg_scale(p.seg, n_base + jr) : p.out_scale);
-    if (p.swiglu) yv = silu_mul(yv, u * p.out_scale_up);
-    const int64_t off = static_cast<int64_t>(m) * n_out + n_base + jr;
+    float y0 = v0 * (p.seg.n ? seg_scale(p.seg, n_base + jr) : p.out_scale);
+    float y1 = v1 * (p.seg.n ? seg_scale(p.seg, n_base + jr + 1) : p.out_scale);
+    if (p.swiglu) {
+      y0 = silu_mul(y0, u0 * p.out_scale_up);
+      y1 = silu_mul(y1, u1 * p.out_scale_up);
+    }
+    const int64_t off = static_cast<int64_t>(m) * n_out + n_base + jr;   // even
     if (p.out_f32) {
-      static_cast<float*>(p.y)[off] = yv;
-      if (p.y_host) static_cast<float*>(p.y_host)[off] = yv;
+      *reinterpret_cast<float2*>(static_cast<float*>(p.y) + off) = make_float2(y0, y1);
+      if (p.y_host)
+        *reinterpret_cast<float2*>(static_cast<float*>(p.y_host) + off) = make_float2(y0, y1);
     } else {
-      const __nv_bfloat16 yb = __float2bfloat16_rn(yv);
-      static_cast<__nv_bfloat16*>(p.y)[off] = yb;
-      if (p.y_host) static_cast<__nv_bfloat16*>(p.y_host)[off] = yb;
+      const uint32_t yb = f32x2_to_bf16x2(y0, y1);
+      *reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(p.y) + off) = yb;
+      if (p.y_host) *reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(p.y_host) + off) = yb;
     }
   };
   if (split == 1) {
     __syncthreads();
-    for (int i = threadIdx.x; i < items; i += kThreads)
-      emit(i, local_part(i, 0), p.swiglu ? local_part(i, 1) : 0.f);
+    for (int i = 2 * threadIdx.x; i < items; i += 2 * kThreads)
+      emit2(i, local_part(i, 0), local_part(i + 1, 0), p.swiglu ? local_part(i, 1) : 0.f,
+            p.swiglu ? local_part(i + 1, 1) : 0.f);
     return;
   }
-  // k split: CTA z owns the items [begin(z), begin(z + 1)).  Each CTA pushes
-  // its partial values of the other CTAs' items into their receive areas
-  // (remote stores, so no thread waits on a remote round trip), one cluster
-  // barrier makes them visible, and each CTA adds its own items' values in
-  // rank order, from local shared memory.  (Reconverge each warp before a
-  // cluster barrier: it is a warp-aligned op.)
-  auto begin = [&](int r) { return static_cast<int>((int64_t)items * r / split); };
-  const int share_max = (items + split - 1) / split;
+  // k split: CTA z owns the items [begin(z), begin(z + 1)) (even bounds, so
+  // that pairs stay whole).  Each CTA pushes its partial values of the other
+  // CTAs' items into their receive areas (remote stores, so no thread waits
+  // on a remote round trip), one cluster barrier makes them visible, and
+  // each CTA adds its own items' values in rank order, from local shared
+  // memory.  (Reconverge each warp before a cluster barrier: it is a
+  // warp-aligned op.)
+  auto begin = [&](int r) { return static_cast<int>((int64_t)items * r / split) & ~1; };
+  const int share_max = ((items + split - 1) / split + 3) & ~1;   // even, >= every share
   float* recv = part + kRows * kPitch;                   // [split][nv][share_max]
   __syncwarp();
   cluster_sync();     // every partial is final and every ring is free
@@ -485,21 +497,26 @@ __global__ void __launch_bounds__(Roles<NM, NI>::kThreads, Roles<NM, NI>::kCtasP
     if (r == z) continue;
     const int b = begin(r), e = begin(r + 1);
     const uint32_t dst = map_to_rank(smem_addr(recv), static_cast<uint32_t>(r));
-    for (int i = b + threadIdx.x; i < e; i += kThreads)
+    for (int i = b + 2 * threadIdx.x; i < e; i += 2 * kThreads)
       for (int c = 0; c < nv; ++c)
-        st_cluster_f32(dst + 4u * static_cast<uint32_t>((z * nv + c) * share_max + (i - b)),
-                       local_part(i, c));
+        st_cluster_f32x2(dst + 4u * static_cast<uint32_t>((z * nv + c) * share_max + (i - b)),
+                         local_part(i, c), local_part(i + 1, c));
   }
   __syncwarp();
   cluster_sync();     // every push has landed; nothing reads remote memory after this
   const int b = begin(z), e = begin(z + 1);
-  for (int i = b + threadIdx.x; i < e; i += kThreads) {
-    float v = 0.f, u = 0.f;
+  for (int i = b + 2 * threadIdx.x; i < e; i += 2 * kThreads) {
+    float v0 = 0.f, v1 = 0.f, u0 = 0.f, u1 = 0.f;
     for (int q = 0; q < split; ++q) {
-      v += q == z ? local_part(i, 0) : recv[(q * nv) * share_max + (i - b)];
-      if (p.swiglu) u += q == z ? local_part(i, 1) : recv[(q * nv + 1) * share_max + (i - b)];
+      const float* rv = recv + (q * nv) * share_max + (i - b);
+      v0 += q == z ? local_part(i, 0) : rv[0];
+      v1 += q == z ? local_part(i + 1, 0) : rv[1];
+      if (p.swiglu) {
+        u0 += q == z ? local_part(i, 1) : rv[share_max];
+        u1 += q == z ? local_part(i + 1, 1) : rv[share_max + 1];
+      }
     }
-    emit(i, v, u);
+    emit2(i, v0, v1, u0, u1);
   }
 }
 
