@@ -88,8 +88,9 @@ extern "C" {
 /* Multiply in bf16, the activations as given (M <= 32): at M <= 8 the
  * warp-MMA few-row kernel in bf16 instead of f16; with NVFP4_FLAG_FORCE_GEMV
  * the bf16 tcgen05 few-row kernel.  (Every default for M = 9..32 is already
- * bf16: the bf16 tcgen05 kernel on weight matrices of N * K >= 2^26, the
- * warp-MMA kernel otherwise.)  Without it, M <= 8 multiplies in f16: code *
+ * bf16: the bf16 tcgen05 kernel on weight matrices of at least 2^27 weights
+ * at M <= 16, 2^26 at M = 17..24 and 3 * 2^23 at M = 25..32, the warp-MMA
+ * kernel otherwise.)  Without it, M <= 8 multiplies in f16: code *
  * scale is exact in f16, and each activation row is brought to f16 after
  * scaling by a power of two taken from the row's running maximum |x|, which
  * is exact for every activation within a factor 2^31 of that maximum; a
