@@ -571,6 +571,9 @@ def test_concurrent_calls_from_two_threads_on_two_streams():
     (1, 0, True), (7, _lib.FLAG_SWIGLU, True), (20, _lib.FLAG_F32_OUT, False),
     (20, _lib.FLAG_F32_OUT, True), (12, _lib.FLAG_SWIGLU | _lib.FLAG_F32_OUT, True),
     (20, _lib.FLAG_FORCE_GEMV | _lib.FLAG_BF16_MMA, True), (12, _lib.FLAG_FORCE_GEMV, True),
+    (9, _lib.FLAG_FORCE_GEMV | _lib.FLAG_BF16_MMA | _lib.FLAG_SWIGLU | _lib.FLAG_F32_OUT |
+     _lib.FLAG_SPLIT(1), True),
+    (32, _lib.FLAG_FORCE_GEMV | _lib.FLAG_BF16_MMA | _lib.FLAG_SWIGLU | _lib.FLAG_SPLIT(3), True),
     (40, 0, True)])
 def test_host_buffer_call_equals_device_call(M, flags, pinned):
     """nvfp4_linear_host (activations and result in host memory, page-locked
